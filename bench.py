@@ -1,0 +1,443 @@
+"""Benchmark of the Mamba-2 SSD chunked forward on one or more GB300s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
+
+A step is one call of ``ssd_chunked_fwd`` (all four stages) on one batch of
+the workload's synthetic inputs, resident in HBM.  Under torchrun every rank
+runs its own batch of the same shape (independent (batch, head) slabs: no
+collective), so ``value`` is the tokens of all ranks over the slowest rank's
+time ("weak" scaling).  Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from state_space_model_gb300 import inputs as gen  # noqa: E402
+
+METRIC = "SSD chunked-forward tokens/s at Mamba-2 2.7B layer shape; % of roofline"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (compulsory HBM bytes, flops) of the path and of each step
+
+
+def path_work(w):
+    B, L, H, P, N, G, Q = (w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups,
+                           w.chunk_size)
+    es = 2 if w.dtype == "bf16" else 4
+    T = B * L
+    rd = T * H * P * es + 2 * T * G * N * es + T * H * 4 + 2 * H * 4
+    if w.init_states:
+        rd += B * H * P * N * 4
+    wr = T * H * P * es + B * H * P * N * 4
+    flops = T * H * (2 * N * P + 2 * N * P + (Q + 1) * P + 2 * N * P / Q) + T * G * (Q + 1) * N
+    return rd + wr, flops
+
+
+def stage_bytes(w):
+    """Bytes each step reads and writes once as a standalone kernel."""
+    B, L, H, P, N, G, Q = (w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups,
+                           w.chunk_size)
+    es = 2 if w.dtype == "bf16" else 4
+    nc = -(-L // Q)
+    T = B * L
+    x, bc, dt = T * H * P * es, T * G * N * es, T * H * 4
+    g = B * H * nc * Q * 4
+    s = B * nc * H * P * N * 4
+    hp = B * nc * H * P * N * es
+    fin = B * H * P * N * 4
+    h0 = fin if w.init_states else 0
+    return {
+        "chunk_cumsum": dt + g,
+        "chunk_state": x + bc + dt + g + s,
+        "state_passing": s + B * H * nc * 4 + h0 + hp + fin,
+        "chunk_scan": x + dt + g + 2 * bc + hp + x,
+    }
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_on = self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.idx)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_on(self):
+        self.t_on = time.time()
+
+    def mark_off(self):
+        self.t_off = time.time()
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((t, float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if self.t_on and self.t_on - 0.15 <= r[0] <= self.t_off + 0.15]
+        use = inside if len(inside) >= 3 else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in use:
+            for name, v in zip(names, r[3][1:5]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use), "reasons": sorted(reasons),
+                "samples": len(use),
+                "window": "timed region" if use is inside else "whole run (timed region too short)"}
+
+
+# ---------------------------------------------------------------------------
+# traffic from a committed ncu summary, valid only for the kernel source it was taken on
+
+
+def kernel_source_hash(stage: str) -> str:
+    csrc = os.path.join(ROOT, "state_space_model_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(stage: str, workload: str):
+    """Per-launch dram read+write bytes recorded in profiles/traffic.txt as
+    `stage workload source_hash bytes`; None if absent or taken on other source."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    want = kernel_source_hash(stage)
+    with open(p) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) == 4 and parts[0] == stage and parts[1] == workload and \
+                    parts[2] == want:
+                return float(parts[3])
+    return None
+
+
+# ---------------------------------------------------------------------------
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if (torch.cuda.is_available() and args.impl == "ours") else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, w, world, rank):
+    """The fp64 oracle on the host cores: each step a bounded sample of the
+    workload's (batch, head) slabs; value = equivalent tokens/s."""
+    if rank != 0:
+        return
+    from oracle import oracle as orc
+    inp = gen.make_inputs(w)
+    cores = orc.max_threads()
+    slabs_all = [(b, h) for b in range(w.batch) for h in range(w.nheads)]
+    t0 = time.perf_counter()
+    orc.recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                   inp["initial_states"], ngroups=w.ngroups, slabs=slabs_all[:cores])
+    per_slab = max((time.perf_counter() - t0) / cores, 1e-4)  # wall per slab at full width
+    budget = 150.0 / max(args.steps + args.warmup, 1)
+    n = int(max(1, min(len(slabs_all), budget / per_slab)))
+    sample = slabs_all[:n]
+    step = lambda: orc.recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                  inp["initial_states"], ngroups=w.ngroups, slabs=sample)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    tokens = n * w.seqlen / w.nheads  # a token is all heads of one position
+    value = tokens / dt
+    desc = f"{n} of {len(slabs_all)} (batch, head) slabs x {w.seqlen} tokens per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen,
+                       "nheads": w.nheads, "headdim": w.headdim, "dstate": w.dstate,
+                       "ngroups": w.ngroups, "chunk_size": w.chunk_size},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, inp):
+    from oracle import oracle as orc
+    cores = orc.max_threads()
+    slabs_all = [(b, h) for b in range(w.batch) for h in range(w.nheads)]
+    # about 10-30 s of CPU work: estimate from a probe of one slab per core
+    t0 = time.perf_counter()
+    orc.recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                   inp["initial_states"], ngroups=w.ngroups, slabs=slabs_all[:cores])
+    per_slab_cpu = (time.perf_counter() - t0)  # core-seconds per slab ~ wall of the probe
+    n = int(max(1, min(len(slabs_all), 20.0 / max(per_slab_cpu, 1e-4))))
+    sample = slabs_all[:n]
+    t0 = time.perf_counter()
+    orc.recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                   inp["initial_states"], ngroups=w.ngroups, slabs=sample)
+    dt = time.perf_counter() - t0
+    return {"value": n * w.seqlen / w.nheads / dt, "unit": "tokens/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{n} of {len(slabs_all)} (batch, head) slabs x {w.seqlen} tokens "
+                      f"({dt:.1f} s wall)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=gen.HEADLINE, choices=sorted(gen.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = gen.WORKLOADS[args.workload]
+    world, rank, local = dist_setup(args)
+
+    if args.impl == "reference":
+        run_reference(args, w, world, rank)
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the CUDA path has no CPU fallback)")
+    from state_space_model_gb300 import build, ssd
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    inp_cpu = gen.make_inputs(w, seed=w.seed + rank)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp_cpu.items()}
+    B, L, H, P, N = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate
+    y = torch.empty((B, L, H, P), dtype=w.torch_dtype, device=dev)
+    fin = torch.empty((B, H, P, N), dtype=torch.float32, device=dev)
+    ws = torch.empty(ssd.workspace_size(B, L, H, P, N, w.ngroups, w.chunk_size, w.torch_dtype),
+                     dtype=torch.uint8, device=dev)
+
+    def step():
+        ssd.chunked_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["initial_states"],
+                        w.chunk_size, w.ngroups, y=y, final_states=fin, workspace=ws)
+
+    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark_on()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_off()
+    barrier(world)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = max_over_ranks(ms, world)
+    clk = clocks.stop()
+    tokens = B * L
+    value = world * tokens / (ms / 1e3)
+
+    # per-step kernel durations: the four stage entry points, events between them
+    nc = -(-L // w.chunk_size)
+    G = torch.empty((B, H, nc * w.chunk_size), dtype=torch.float32, device=dev)
+    S = torch.empty((B, nc, H, P, N), dtype=torch.float32, device=dev)
+    hp = torch.empty((B, nc, H, P, N), dtype=w.torch_dtype, device=dev)
+    kstats = {k: 0.0 for k in ("chunk_cumsum", "chunk_state", "state_passing", "chunk_scan")}
+    reps = max(10, min(args.steps, 200))
+    for it in range(reps + 3):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        evs[0].record(stream)
+        ssd.chunk_cumsum(d["dt"], d["A"], w.chunk_size, out=G)
+        evs[1].record(stream)
+        ssd.chunk_state(d["x"], d["B"], d["dt"], G, w.chunk_size, w.ngroups, out=S)
+        evs[2].record(stream)
+        ssd.state_passing(S, G, d["initial_states"], w.chunk_size, out=(hp, fin))
+        evs[3].record(stream)
+        ssd.chunk_scan(d["x"], d["dt"], G, d["B"], d["C"], d["D"], hp, w.chunk_size, w.ngroups,
+                       out=y)
+        evs[4].record(stream)
+        torch.cuda.synchronize()
+        if it >= 3:
+            for i, k in enumerate(kstats):
+                kstats[k] += evs[i].elapsed_time(evs[i + 1]) / reps
+    dom = max(kstats, key=kstats.get)
+    pk = peaks()
+    sb = stage_bytes(w)
+    achieved = sb[dom] / (kstats[dom] / 1e3) / 1e9
+    traffic = recorded_traffic(dom, w.name)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                "algorithmic_bytes": sb[dom], "kernel_ms": kstats[dom],
+                "peak_source": pk["source"],
+                "kernel_ms_all": {k: round(v, 4) for k, v in kstats.items()}}
+    pbytes, pflops = path_work(w)
+    t_roof = max(pbytes / (pk["hbm_gbs"] * 1e9), pflops / (pk["bf16_tflops"] * 1e12))
+    path_roof = {"t_roof_us": t_roof * 1e6, "t_step_us": ms * 1e3,
+                 "frac": t_roof / (ms / 1e3), "bytes": pbytes, "flops": pflops,
+                 "peak_source": pk["source"]}
+
+    # end to end: pinned host inputs -> device, the call, results -> pinned host
+    e2e = None
+    if not args.no_e2e:
+        host = {k: (None if v is None else v.pin_memory()) for k, v in inp_cpu.items()}
+        y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        f_h = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        d2h = y_h.numel() * y_h.element_size() + f_h.numel() * f_h.element_size()
+
+        def e2e_step():
+            for k, v in host.items():
+                if v is not None:
+                    d[k].copy_(v, non_blocking=True)
+            step()
+            y_h.copy_(y, non_blocking=True)
+            f_h.copy_(fin, non_blocking=True)
+
+        k_e2e = max(10, min(args.steps, 200))
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        ems = max_over_ranks(e0.elapsed_time(e1) / k_e2e, world)
+        e2e = {"value": world * tokens / (ems / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k_e2e,
+               "ms_per_step": ems}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, inp_cpu)
+
+    if rank == 0:
+        in_bytes = sum(v.numel() * v.element_size() for v in inp_cpu.values() if v is not None)
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic (seeded; see state_space_model_gb300/inputs.py)",
+            "config": {"workload": w.name, "batch": B, "seqlen": L, "nheads": H, "headdim": P,
+                       "dstate": N, "ngroups": w.ngroups, "chunk_size": w.chunk_size,
+                       "initial_states": w.init_states, "parallelism": f"replicas{world}",
+                       "l2": (f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > "
+                              f"{L2_BYTES / 1e6:.0f} MB), no flush")
+                       if in_bytes > L2_BYTES else "inputs smaller than L2"},
+            "roofline": roofline, "path_roofline": path_roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 4 * args.steps, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,155 @@
+/*
+ * ssd.h -- C ABI of the GB300 (sm_103a) Mamba-2 SSD chunked forward.
+ *
+ * The operation is the Mamba-2 layer recurrence of "Accelerating Mamba-2 with
+ * High-Performance Forward Pass Kernels in NVIDIA CUDA Tile", section
+ * "Mamba-2 architecture":
+ *
+ *     h_t = exp(A[h] * dt_t) * h_{t-1} + dt_t * x_t (outer) B_t      (P x N state)
+ *     y_t = h_t C_t + D[h] * x_t                                        (updated state)
+ *
+ * evaluated chunk by chunk in four stages (sections "Kernel 1: Computing
+ * cumulative sums", "Kernel 2: fwd_pass_state", "Kernel 3: compute_out"):
+ * chunk_cumsum, chunk_state, state_passing, chunk_scan.  Head h reads group
+ * g = h / (H / G) of B and C.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensors are described by ssd_tensor: a pointer, a dtype, and shape and
+ *   strides in ELEMENTS.  The innermost stride must be 1.  Pointers passed
+ *   to the compute entry points are DEVICE pointers of the current device.
+ * - Shapes (B batch, L seqlen, H nheads, P headdim, N dstate, G ngroups,
+ *   Q chunk_size, nc = ceil(L / Q)):
+ *     x  [B, L, H, P]  bf16 or f32        dt [B, L, H] f32 (post-softplus, >= 0)
+ *     A  [H]           f32 (<= 0)         D  [H] f32, optional (absent = 0)
+ *     B  [B, L, G, N]  dtype of x         C  [B, L, G, N] dtype of x
+ *     initial_states [B, H, P, N] f32, optional (absent = 0)
+ *     y  [B, L, H, P]  dtype of x         final_states [B, H, P, N] f32, optional
+ *   The sign conditions on dt and A are the method's premises (every kept
+ *   exponent is <= 0); they are documented, not checked.
+ * - Supported geometry: P and N in {16, 32, 64, 128}; Q in {64, 128, 256};
+ *   H a multiple of G.  Anything else returns SSD_ERR_UNSUPPORTED.
+ * - Alignment: every base pointer 16-byte aligned; for x, B, C and y every
+ *   outer stride a multiple of 16 bytes.  Violations return SSD_ERR_ALIGNMENT.
+ * - Ownership: the caller owns every buffer, workspace included.  The library
+ *   never allocates, frees or synchronises; all work is enqueued in order on
+ *   `stream` and returns asynchronously.  Inputs must stay alive until the
+ *   stream passes this call.  `stream` is a cudaStream_t (NULL = the legacy
+ *   default stream).
+ * - Errors: every check runs on the host before any launch; on failure the
+ *   call returns a status, launches nothing, and ssd_last_error_detail()
+ *   names the check and its figures.  A launch failure returns SSD_ERR_CUDA.
+ *   No C++ exception crosses this boundary.
+ * - Aliasing: outputs must not overlap inputs (checked by address range).
+ * - Results are deterministic: repeated calls give bitwise-identical outputs
+ *   (no floating-point atomics).
+ */
+#ifndef SSD_GB300_H
+#define SSD_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1, /* null pointer, bad shape, dtype or aliasing  */
+    SSD_ERR_UNSUPPORTED = 2, /* valid but outside the supported geometry     */
+    SSD_ERR_ALIGNMENT = 3,   /* pointer or stride alignment                  */
+    SSD_ERR_WORKSPACE = 4,   /* workspace missing or too small               */
+    SSD_ERR_CUDA = 5,        /* a CUDA runtime or launch error               */
+    SSD_ERR_TIMEOUT = 6      /* a device-side bounded wait gave up           */
+} ssd_status;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+typedef struct {
+    void *data;          /* device pointer                                   */
+    int32_t dtype;       /* ssd_dtype                                        */
+    int32_t ndim;        /* number of valid entries in shape / stride        */
+    int64_t shape[5];
+    int64_t stride[5];   /* in elements                                      */
+} ssd_tensor;
+
+/* Human-readable name of a status code (static storage). */
+const char *ssd_status_string(ssd_status status);
+
+/* Text of the last failed check on the calling thread (thread-local storage,
+ * valid until the next call on that thread); "" after a successful call. */
+const char *ssd_last_error_detail(void);
+
+/* Bytes of device workspace ssd_chunked_fwd needs for this problem, written
+ * to *bytes.  x_dtype is the ssd_dtype of x, B, C.  The workspace holds the
+ * scaled in-chunk cumulative sums G [B, H, nc*Q] f32, the per-chunk states
+ * [B, nc, H, P, N] f32 and the chunk-entering states [B, nc, H, P, N] in the
+ * dtype of x.  Returns SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED for shapes
+ * ssd_chunked_fwd would reject. */
+ssd_status ssd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads,
+                              int64_t headdim, int64_t dstate, int64_t ngroups,
+                              int64_t chunk_size, int32_t x_dtype,
+                              size_t *bytes);
+
+/* The SSD chunked forward: y and (optionally) final_states from x, dt, A, B,
+ * C, D, initial_states, as defined at the top of this file.  A sequence
+ * length that is not a multiple of chunk_size is handled as if zero-padded
+ * (dt = x = B = C = 0 on the padding), which changes nothing; only the L real
+ * tokens of y are written.  D, initial_states and final_states may be NULL.
+ * workspace: device memory of at least ssd_workspace_size() bytes, 256-byte
+ * aligned, owned by the caller; its contents on entry are ignored. */
+ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt,
+                           const ssd_tensor *A, const ssd_tensor *B,
+                           const ssd_tensor *C, const ssd_tensor *D,
+                           const ssd_tensor *initial_states,
+                           int64_t chunk_size, int64_t ngroups,
+                           ssd_tensor *y, ssd_tensor *final_states,
+                           void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/* ---- stage entry points (the four steps of ssd_chunked_fwd, one call each;
+ *      same conventions; used to check each step on its own) ---------------- */
+
+/* Step 1, "Kernel 1: Computing cumulative sums": for every chunk c,
+ *   G[b, h, c*Q + k] = log2(e) * sum_{k' <= k} A[h] * dt[b, c*Q + k', h]
+ * over the zero-padded sequence (so positions past L repeat the chunk's last
+ * real value).  G: [B, H, nc*Q] f32, contiguous. */
+ssd_status ssd_stage_chunk_cumsum(const ssd_tensor *dt, const ssd_tensor *A,
+                                  int64_t chunk_size, ssd_tensor *G,
+                                  void *stream);
+
+/* Step 2, the jump formula of "Kernel 2: fwd_pass_state" without the carried
+ * state: the state one chunk leaves behind when it starts from zero,
+ *   S[b, c, h, p, n] = sum_{j in chunk c} 2^(G_last - G_j) dt_j x_j[p] B_j[n]
+ * with G_last = G[b, h, c*Q + Q - 1].  S: [B, nc, H, P, N] f32, contiguous. */
+ssd_status ssd_stage_chunk_state(const ssd_tensor *x, const ssd_tensor *B,
+                                 const ssd_tensor *dt, const ssd_tensor *G,
+                                 int64_t chunk_size, int64_t ngroups,
+                                 ssd_tensor *S, void *stream);
+
+/* Step 3, the sequential loop of "Kernel 2: fwd_pass_state": for each (b, h),
+ *   h_prev[0] = initial_states (or 0),
+ *   h_prev[c+1] = 2^(G_last,c) h_prev[c] + S[c],   final = h_prev[nc]
+ * in fp32.  h_prev: [B, nc, H, P, N] f32 or bf16 (stored rounded), contiguous;
+ * final_states may be NULL. */
+ssd_status ssd_stage_state_passing(const ssd_tensor *S, const ssd_tensor *G,
+                                   const ssd_tensor *initial_states,
+                                   int64_t chunk_size, ssd_tensor *h_prev,
+                                   ssd_tensor *final_states, void *stream);
+
+/* Step 4, "Kernel 3: compute_out": per chunk,
+ *   Y = 2^G (C h_prev^T) + (2^(G_i - G_j) (C B^T)_ij [j <= i]) (dt x) + D x
+ * with the causal selection taken before any exponent is used.  h_prev must
+ * have the dtype of x for bf16 inputs and f32 for f32 inputs. */
+ssd_status ssd_stage_chunk_scan(const ssd_tensor *x, const ssd_tensor *dt,
+                                const ssd_tensor *G, const ssd_tensor *B,
+                                const ssd_tensor *C, const ssd_tensor *D,
+                                const ssd_tensor *h_prev, int64_t chunk_size,
+                                int64_t ngroups, ssd_tensor *y, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_GB300_H */

@@ -1,0 +1,508 @@
+// Host side of the C ABI declared in include/ssd.h: argument checks, the
+// workspace plan and the ordered launch of the four steps on the caller's
+// stream.  Every check runs before the first launch; nothing here allocates,
+// frees or synchronises.
+#include "ssd.h"
+#include "ssd_internal.h"
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <initializer_list>
+#include <string>
+
+namespace {
+
+thread_local std::string g_detail;
+
+ssd_status fail(ssd_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_detail = buf;
+    return st;
+}
+
+ssd_status ok() {
+    g_detail.clear();
+    return SSD_OK;
+}
+
+size_t elem_size(int dt) { return dt == SSD_F32 ? 4 : 2; }
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+bool supported_dim(int64_t v) { return v == 16 || v == 32 || v == 64 || v == 128; }
+bool supported_chunk(int64_t q) { return q == 64 || q == 128 || q == 256; }
+
+// Address range [lo, hi) a tensor touches; empty when any extent is 0.
+struct Range {
+    uintptr_t lo = 0, hi = 0;
+};
+Range range_of(const ssd_tensor *t) {
+    Range r;
+    if (!t || !t->data) return r;
+    int64_t last = 0;
+    for (int i = 0; i < t->ndim; ++i) {
+        if (t->shape[i] == 0) return r;
+        last += (t->shape[i] - 1) * t->stride[i];
+    }
+    r.lo = reinterpret_cast<uintptr_t>(t->data);
+    r.hi = r.lo + size_t(last + 1) * elem_size(t->dtype);
+    return r;
+}
+Range range_raw(const void *p, size_t bytes) {
+    Range r;
+    if (p && bytes) {
+        r.lo = reinterpret_cast<uintptr_t>(p);
+        r.hi = r.lo + bytes;
+    }
+    return r;
+}
+bool overlap(Range a, Range b) {
+    return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi;
+}
+
+// Checks one tensor's rank, dtype, shape, unit inner stride and alignment.
+// dtype < 0 accepts f32 or bf16.  contiguous demands packed row-major strides.
+ssd_status check_tensor(const ssd_tensor *t, const char *name, int ndim,
+                        const int64_t *shape, int dtype, bool contiguous,
+                        bool align_strides16) {
+    if (!t) return fail(SSD_ERR_INVALID_ARG, "%s: null tensor descriptor", name);
+    if (t->ndim != ndim)
+        return fail(SSD_ERR_INVALID_ARG, "%s: ndim %d, expected %d", name, t->ndim, ndim);
+    if (t->dtype != SSD_F32 && t->dtype != SSD_BF16)
+        return fail(SSD_ERR_INVALID_ARG, "%s: unknown dtype code %d", name, t->dtype);
+    if (dtype >= 0 && t->dtype != dtype)
+        return fail(SSD_ERR_INVALID_ARG, "%s: dtype %s, expected %s", name,
+                    t->dtype == SSD_F32 ? "f32" : "bf16", dtype == SSD_F32 ? "f32" : "bf16");
+    int64_t numel = 1;
+    for (int i = 0; i < ndim; ++i) {
+        if (t->shape[i] != shape[i])
+            return fail(SSD_ERR_INVALID_ARG, "%s: shape[%d] = %lld, expected %lld", name, i,
+                        (long long)t->shape[i], (long long)shape[i]);
+        numel *= shape[i];
+    }
+    if (numel > 0 && !t->data) return fail(SSD_ERR_INVALID_ARG, "%s: null data pointer", name);
+    if (t->stride[ndim - 1] != 1 && shape[ndim - 1] > 1)
+        return fail(SSD_ERR_INVALID_ARG, "%s: innermost stride %lld, must be 1", name,
+                    (long long)t->stride[ndim - 1]);
+    if (contiguous) {
+        int64_t want = 1;
+        for (int i = ndim - 1; i >= 0; --i) {
+            if (shape[i] > 1 && t->stride[i] != want)
+                return fail(SSD_ERR_INVALID_ARG, "%s: must be contiguous (stride[%d] = %lld, "
+                            "expected %lld)", name, i, (long long)t->stride[i], (long long)want);
+            want *= shape[i];
+        }
+    }
+    for (int i = 0; i < ndim - 1; ++i)
+        if (t->stride[i] < 0)
+            return fail(SSD_ERR_INVALID_ARG, "%s: negative stride", name);
+    const size_t es = elem_size(t->dtype);
+    if (numel > 0 && (reinterpret_cast<uintptr_t>(t->data) % (align_strides16 ? 16 : es)))
+        return fail(SSD_ERR_ALIGNMENT, "%s: base pointer %p not %zu-byte aligned", name, t->data,
+                    align_strides16 ? size_t(16) : es);
+    if (align_strides16)
+        for (int i = 0; i < ndim - 1; ++i)
+            if (shape[i] > 1 && (t->stride[i] * int64_t(es)) % 16)
+                return fail(SSD_ERR_ALIGNMENT, "%s: stride[%d] = %lld elements is not a multiple "
+                            "of 16 bytes", name, i, (long long)t->stride[i]);
+    return SSD_OK;
+}
+
+ssd_status check_geometry(int64_t B, int64_t L, int64_t H, int64_t P, int64_t N, int64_t G,
+                          int64_t Q) {
+    if (B < 0 || L < 0) return fail(SSD_ERR_INVALID_ARG, "batch %lld / seqlen %lld negative",
+                                    (long long)B, (long long)L);
+    if (H <= 0 || G <= 0) return fail(SSD_ERR_INVALID_ARG, "nheads %lld / ngroups %lld must be "
+                                      "positive", (long long)H, (long long)G);
+    if (H % G) return fail(SSD_ERR_INVALID_ARG, "nheads %lld is not a multiple of ngroups %lld",
+                           (long long)H, (long long)G);
+    if (Q <= 0) return fail(SSD_ERR_INVALID_ARG, "chunk_size %lld must be positive", (long long)Q);
+    if (!supported_chunk(Q))
+        return fail(SSD_ERR_UNSUPPORTED, "chunk_size %lld unsupported (64, 128 or 256)",
+                    (long long)Q);
+    if (!supported_dim(P))
+        return fail(SSD_ERR_UNSUPPORTED, "headdim %lld unsupported (16, 32, 64 or 128)",
+                    (long long)P);
+    if (!supported_dim(N))
+        return fail(SSD_ERR_UNSUPPORTED, "dstate %lld unsupported (16, 32, 64 or 128)",
+                    (long long)N);
+    if (B > 65535 || H > 65535)
+        return fail(SSD_ERR_UNSUPPORTED, "batch %lld or nheads %lld above 65535", (long long)B,
+                    (long long)H);
+    const int64_t nc = (L + Q - 1) / Q;
+    if (nc > (int64_t(1) << 30))
+        return fail(SSD_ERR_UNSUPPORTED, "seqlen %lld too long", (long long)L);
+    return SSD_OK;
+}
+
+struct Plan {
+    size_t off_G, off_S, off_hp, total;
+};
+
+Plan plan_workspace(const ssd::Dims &d, int xdt) {
+    Plan p{};
+    const size_t g = size_t(d.B) * d.H * d.nc * d.Q * 4;
+    const size_t s = size_t(d.B) * d.nc * d.H * d.P * d.N * 4;
+    const size_t hp = size_t(d.B) * d.nc * d.H * d.P * d.N * elem_size(xdt);
+    p.off_G = 0;
+    p.off_S = align256(p.off_G + g);
+    p.off_hp = align256(p.off_S + s);
+    p.total = align256(p.off_hp + hp);
+    return p;
+}
+
+// Every data pointer must be device (or managed) memory of the current
+// device: a host pointer handed to a kernel would fault it.  Runs after all
+// pure-host checks, so argument errors are reported without touching CUDA.
+struct NamedPtr {
+    const void *p;
+    const char *name;
+};
+ssd_status check_device_ptrs(std::initializer_list<NamedPtr> ptrs) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    for (const NamedPtr &np : ptrs) {
+        if (!np.p) continue;
+        cudaPointerAttributes at{};
+        e = cudaPointerGetAttributes(&at, np.p);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(SSD_ERR_INVALID_ARG, "%s: pointer %p is not CUDA memory (%s)", np.name,
+                        np.p, cudaGetErrorString(e));
+        }
+        if (at.type == cudaMemoryTypeManaged) continue;
+        if (at.type != cudaMemoryTypeDevice)
+            return fail(SSD_ERR_INVALID_ARG, "%s: pointer %p is host memory; device memory is "
+                        "required", np.name, np.p);
+        if (at.device != dev)
+            return fail(SSD_ERR_INVALID_ARG, "%s: pointer on device %d, current device is %d",
+                        np.name, at.device, dev);
+    }
+    return SSD_OK;
+}
+
+ssd_status cuda_status(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return SSD_OK;
+    return fail(SSD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+void fill_x(ssd::Args &a, const ssd_tensor *x) {
+    a.x = x->data;
+    a.x_sb = x->stride[0];
+    a.x_sl = x->stride[1];
+    a.x_sh = x->stride[2];
+}
+void fill_dt(ssd::Args &a, const ssd_tensor *dt) {
+    a.dt = static_cast<const float *>(dt->data);
+    a.dt_sb = dt->stride[0];
+    a.dt_sl = dt->stride[1];
+}
+void fill_bc(ssd::Args &a, const ssd_tensor *Bm, const ssd_tensor *Cm) {
+    if (Bm) {
+        a.Bm = Bm->data;
+        a.b_sb = Bm->stride[0];
+        a.b_sl = Bm->stride[1];
+        a.b_sg = Bm->stride[2];
+    }
+    if (Cm) {
+        a.Cm = Cm->data;
+        a.c_sb = Cm->stride[0];
+        a.c_sl = Cm->stride[1];
+        a.c_sg = Cm->stride[2];
+    }
+}
+void fill_y(ssd::Args &a, ssd_tensor *y) {
+    a.y = y->data;
+    a.y_sb = y->stride[0];
+    a.y_sl = y->stride[1];
+    a.y_sh = y->stride[2];
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ssd_status_string(ssd_status s) {
+    switch (s) {
+        case SSD_OK: return "SSD_OK";
+        case SSD_ERR_INVALID_ARG: return "SSD_ERR_INVALID_ARG";
+        case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED";
+        case SSD_ERR_ALIGNMENT: return "SSD_ERR_ALIGNMENT";
+        case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE";
+        case SSD_ERR_CUDA: return "SSD_ERR_CUDA";
+        case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT";
+    }
+    return "SSD_UNKNOWN_STATUS";
+}
+
+const char *ssd_last_error_detail(void) { return g_detail.c_str(); }
+
+ssd_status ssd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                              int64_t dstate, int64_t ngroups, int64_t chunk_size,
+                              int32_t x_dtype, size_t *bytes) {
+    if (!bytes) return fail(SSD_ERR_INVALID_ARG, "bytes: null pointer");
+    *bytes = 0;
+    if (x_dtype != SSD_F32 && x_dtype != SSD_BF16)
+        return fail(SSD_ERR_INVALID_ARG, "x_dtype: unknown dtype code %d", x_dtype);
+    ssd_status st = check_geometry(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size);
+    if (st != SSD_OK) return st;
+    ssd::Dims d{batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size,
+                (seqlen + chunk_size - 1) / chunk_size};
+    *bytes = plan_workspace(d, x_dtype).total;
+    return ok();
+}
+
+ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt, const ssd_tensor *A,
+                           const ssd_tensor *Bm, const ssd_tensor *Cm, const ssd_tensor *D,
+                           const ssd_tensor *h0, int64_t chunk_size, int64_t ngroups,
+                           ssd_tensor *y, ssd_tensor *final_states, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    if (!x) return fail(SSD_ERR_INVALID_ARG, "x: null tensor descriptor");
+    if (x->ndim != 4) return fail(SSD_ERR_INVALID_ARG, "x: ndim %d, expected 4", x->ndim);
+    if (!Bm) return fail(SSD_ERR_INVALID_ARG, "B: null tensor descriptor");
+    if (Bm->ndim != 4) return fail(SSD_ERR_INVALID_ARG, "B: ndim %d, expected 4", Bm->ndim);
+    const int64_t Bn = x->shape[0], L = x->shape[1], H = x->shape[2], P = x->shape[3];
+    const int64_t N = Bm->shape[3], G = ngroups, Q = chunk_size;
+    ssd_status st = check_geometry(Bn, L, H, P, N, G, Q);
+    if (st != SSD_OK) return st;
+    const int xdt = x->dtype;
+    const int64_t sx[4] = {Bn, L, H, P}, sdt[3] = {Bn, L, H}, sh[1] = {H},
+                  sbc[4] = {Bn, L, G, N}, sst[4] = {Bn, H, P, N};
+    if ((st = check_tensor(x, "x", 4, sx, -1, false, true))) return st;
+    if ((st = check_tensor(dt, "dt", 3, sdt, SSD_F32, false, false))) return st;
+    if ((st = check_tensor(A, "A", 1, sh, SSD_F32, true, false))) return st;
+    if ((st = check_tensor(Bm, "B", 4, sbc, xdt, false, true))) return st;
+    if ((st = check_tensor(Cm, "C", 4, sbc, xdt, false, true))) return st;
+    if (D && (st = check_tensor(D, "D", 1, sh, SSD_F32, true, false))) return st;
+    if (h0 && (st = check_tensor(h0, "initial_states", 4, sst, SSD_F32, true, true))) return st;
+    if ((st = check_tensor(y, "y", 4, sx, xdt, false, true))) return st;
+    if (final_states &&
+        (st = check_tensor(final_states, "final_states", 4, sst, SSD_F32, true, true)))
+        return st;
+
+    ssd::Dims d{Bn, L, H, P, N, G, Q, (L + Q - 1) / Q};
+    const Plan plan = plan_workspace(d, xdt);
+    if (Bn > 0) {
+        if (workspace_bytes < plan.total)
+            return fail(SSD_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes,
+                        plan.total);
+        if (!workspace) return fail(SSD_ERR_WORKSPACE, "workspace: null pointer");
+        if (reinterpret_cast<uintptr_t>(workspace) % 256)
+            return fail(SSD_ERR_ALIGNMENT, "workspace %p not 256-byte aligned", workspace);
+    }
+
+    const Range ins[] = {range_of(x), range_of(dt), range_of(A), range_of(Bm), range_of(Cm),
+                         range_of(D), range_of(h0)};
+    const char *in_names[] = {"x", "dt", "A", "B", "C", "D", "initial_states"};
+    const Range ry = range_of(y), rf = range_of(final_states);
+    const Range rw = range_raw(workspace, Bn > 0 ? plan.total : 0);
+    for (int i = 0; i < 7; ++i) {
+        if (overlap(ry, ins[i])) return fail(SSD_ERR_INVALID_ARG, "y overlaps %s", in_names[i]);
+        if (overlap(rf, ins[i]))
+            return fail(SSD_ERR_INVALID_ARG, "final_states overlaps %s", in_names[i]);
+        if (overlap(rw, ins[i]))
+            return fail(SSD_ERR_INVALID_ARG, "workspace overlaps %s", in_names[i]);
+    }
+    if (overlap(ry, rf)) return fail(SSD_ERR_INVALID_ARG, "y overlaps final_states");
+    if (overlap(rw, ry) || overlap(rw, rf))
+        return fail(SSD_ERR_INVALID_ARG, "workspace overlaps an output");
+    if (Bn == 0) return ok();
+    auto dp = [](const ssd_tensor *t) -> const void * { return t ? t->data : nullptr; };
+    if ((st = check_device_ptrs({{dp(x), "x"}, {dp(dt), "dt"}, {dp(A), "A"}, {dp(Bm), "B"},
+                                 {dp(Cm), "C"}, {dp(D), "D"}, {dp(h0), "initial_states"},
+                                 {dp(y), "y"}, {dp(final_states), "final_states"},
+                                 {workspace, "workspace"}})))
+        return st;
+
+    ssd::Args a;
+    a.d = d;
+    a.xdt = xdt;
+    fill_x(a, x);
+    fill_dt(a, dt);
+    a.A = static_cast<const float *>(A->data);
+    a.D = D ? static_cast<const float *>(D->data) : nullptr;
+    fill_bc(a, Bm, Cm);
+    a.h0 = h0 ? static_cast<const float *>(h0->data) : nullptr;
+    fill_y(a, y);
+    a.final_states = final_states ? static_cast<float *>(final_states->data) : nullptr;
+    char *ws = static_cast<char *>(workspace);
+    a.G = reinterpret_cast<float *>(ws + plan.off_G);
+    a.S = reinterpret_cast<float *>(ws + plan.off_S);
+    a.h_prev = ws + plan.off_hp;
+    a.hprev_dt = xdt;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (L > 0) {
+        if ((st = cuda_status(ssd::launch_chunk_cumsum(a, s), "chunk_cumsum"))) return st;
+        if ((st = cuda_status(ssd::launch_chunk_state(a, s), "chunk_state"))) return st;
+    }
+    if ((st = cuda_status(ssd::launch_state_passing(a, s), "state_passing"))) return st;
+    if (L > 0 && (st = cuda_status(ssd::launch_chunk_scan(a, s), "chunk_scan"))) return st;
+    return ok();
+}
+
+ssd_status ssd_stage_chunk_cumsum(const ssd_tensor *dt, const ssd_tensor *A, int64_t chunk_size,
+                                  ssd_tensor *G, void *stream) {
+    if (!dt) return fail(SSD_ERR_INVALID_ARG, "dt: null tensor descriptor");
+    if (dt->ndim != 3) return fail(SSD_ERR_INVALID_ARG, "dt: ndim %d, expected 3", dt->ndim);
+    const int64_t Bn = dt->shape[0], L = dt->shape[1], H = dt->shape[2], Q = chunk_size;
+    ssd_status st = check_geometry(Bn, L, H, 64, 64, 1, Q);
+    if (st != SSD_OK) return st;
+    const int64_t nc = (L + Q - 1) / Q;
+    const int64_t sdt[3] = {Bn, L, H}, sh[1] = {H}, sg[3] = {Bn, H, nc * Q};
+    if ((st = check_tensor(dt, "dt", 3, sdt, SSD_F32, false, false))) return st;
+    if ((st = check_tensor(A, "A", 1, sh, SSD_F32, true, false))) return st;
+    if ((st = check_tensor(G, "G", 3, sg, SSD_F32, true, false))) return st;
+    if (overlap(range_of(G), range_of(dt)) || overlap(range_of(G), range_of(A)))
+        return fail(SSD_ERR_INVALID_ARG, "G overlaps an input");
+    if (Bn == 0 || L == 0) return ok();
+    if ((st = check_device_ptrs({{dt->data, "dt"}, {A->data, "A"}, {G->data, "G"}}))) return st;
+    ssd::Args a;
+    a.d = ssd::Dims{Bn, L, H, 64, 64, 1, Q, nc};
+    fill_dt(a, dt);
+    a.A = static_cast<const float *>(A->data);
+    a.G = static_cast<float *>(G->data);
+    if ((st = cuda_status(ssd::launch_chunk_cumsum(a, static_cast<cudaStream_t>(stream)),
+                          "chunk_cumsum")))
+        return st;
+    return ok();
+}
+
+ssd_status ssd_stage_chunk_state(const ssd_tensor *x, const ssd_tensor *Bm, const ssd_tensor *dt,
+                                 const ssd_tensor *G, int64_t chunk_size, int64_t ngroups,
+                                 ssd_tensor *S, void *stream) {
+    if (!x || !Bm) return fail(SSD_ERR_INVALID_ARG, "x / B: null tensor descriptor");
+    if (x->ndim != 4 || Bm->ndim != 4) return fail(SSD_ERR_INVALID_ARG, "x / B: ndim must be 4");
+    const int64_t Bn = x->shape[0], L = x->shape[1], H = x->shape[2], P = x->shape[3];
+    const int64_t N = Bm->shape[3], Gn = ngroups, Q = chunk_size;
+    ssd_status st = check_geometry(Bn, L, H, P, N, Gn, Q);
+    if (st != SSD_OK) return st;
+    const int64_t nc = (L + Q - 1) / Q;
+    const int64_t sx[4] = {Bn, L, H, P}, sdt[3] = {Bn, L, H}, sbc[4] = {Bn, L, Gn, N},
+                  sg[3] = {Bn, H, nc * Q}, ss[5] = {Bn, nc, H, P, N};
+    if ((st = check_tensor(x, "x", 4, sx, -1, false, true))) return st;
+    if ((st = check_tensor(Bm, "B", 4, sbc, x->dtype, false, true))) return st;
+    if ((st = check_tensor(dt, "dt", 3, sdt, SSD_F32, false, false))) return st;
+    if ((st = check_tensor(G, "G", 3, sg, SSD_F32, true, false))) return st;
+    if ((st = check_tensor(S, "S", 5, ss, SSD_F32, true, true))) return st;
+    const Range rs = range_of(S);
+    if (overlap(rs, range_of(x)) || overlap(rs, range_of(Bm)) || overlap(rs, range_of(dt)) ||
+        overlap(rs, range_of(G)))
+        return fail(SSD_ERR_INVALID_ARG, "S overlaps an input");
+    if (Bn == 0 || L == 0) return ok();
+    if ((st = check_device_ptrs({{x->data, "x"}, {Bm->data, "B"}, {dt->data, "dt"},
+                                 {G->data, "G"}, {S->data, "S"}})))
+        return st;
+    ssd::Args a;
+    a.d = ssd::Dims{Bn, L, H, P, N, Gn, Q, nc};
+    a.xdt = x->dtype;
+    fill_x(a, x);
+    fill_bc(a, Bm, nullptr);
+    fill_dt(a, dt);
+    a.G = static_cast<float *>(G->data);
+    a.S = static_cast<float *>(S->data);
+    if ((st = cuda_status(ssd::launch_chunk_state(a, static_cast<cudaStream_t>(stream)),
+                          "chunk_state")))
+        return st;
+    return ok();
+}
+
+ssd_status ssd_stage_state_passing(const ssd_tensor *S, const ssd_tensor *G,
+                                   const ssd_tensor *h0, int64_t chunk_size, ssd_tensor *h_prev,
+                                   ssd_tensor *final_states, void *stream) {
+    if (!S) return fail(SSD_ERR_INVALID_ARG, "S: null tensor descriptor");
+    if (S->ndim != 5) return fail(SSD_ERR_INVALID_ARG, "S: ndim %d, expected 5", S->ndim);
+    if (!G || G->ndim != 3) return fail(SSD_ERR_INVALID_ARG, "G: missing or ndim != 3");
+    const int64_t Bn = S->shape[0], nc = S->shape[1], H = S->shape[2], P = S->shape[3],
+                  N = S->shape[4], Q = chunk_size;
+    ssd_status st = check_geometry(Bn, nc * Q, H, P, N, 1, Q);
+    if (st != SSD_OK) return st;
+    const int64_t ss[5] = {Bn, nc, H, P, N}, sg[3] = {Bn, H, nc * Q}, sst[4] = {Bn, H, P, N};
+    if ((st = check_tensor(S, "S", 5, ss, SSD_F32, true, true))) return st;
+    if ((st = check_tensor(G, "G", 3, sg, SSD_F32, true, false))) return st;
+    if (h0 && (st = check_tensor(h0, "initial_states", 4, sst, SSD_F32, true, true))) return st;
+    if ((st = check_tensor(h_prev, "h_prev", 5, ss, -1, true, true))) return st;
+    if (final_states &&
+        (st = check_tensor(final_states, "final_states", 4, sst, SSD_F32, true, true)))
+        return st;
+    const Range rh = range_of(h_prev), rf = range_of(final_states);
+    const Range ins[] = {range_of(S), range_of(G), range_of(h0)};
+    for (const Range &r : ins)
+        if (overlap(rh, r) || overlap(rf, r))
+            return fail(SSD_ERR_INVALID_ARG, "an output overlaps an input");
+    if (overlap(rh, rf)) return fail(SSD_ERR_INVALID_ARG, "h_prev overlaps final_states");
+    if (Bn == 0) return ok();
+    if ((st = check_device_ptrs({{S->data, "S"}, {G->data, "G"},
+                                 {h0 ? h0->data : nullptr, "initial_states"},
+                                 {h_prev->data, "h_prev"},
+                                 {final_states ? final_states->data : nullptr, "final_states"}})))
+        return st;
+    ssd::Args a;
+    a.d = ssd::Dims{Bn, nc * Q, H, P, N, 1, Q, nc};
+    a.S = static_cast<float *>(S->data);
+    a.G = static_cast<float *>(G->data);
+    a.h0 = h0 ? static_cast<const float *>(h0->data) : nullptr;
+    a.h_prev = h_prev->data;
+    a.hprev_dt = h_prev->dtype;
+    a.final_states = final_states ? static_cast<float *>(final_states->data) : nullptr;
+    if ((st = cuda_status(ssd::launch_state_passing(a, static_cast<cudaStream_t>(stream)),
+                          "state_passing")))
+        return st;
+    return ok();
+}
+
+ssd_status ssd_stage_chunk_scan(const ssd_tensor *x, const ssd_tensor *dt, const ssd_tensor *G,
+                                const ssd_tensor *Bm, const ssd_tensor *Cm, const ssd_tensor *D,
+                                const ssd_tensor *h_prev, int64_t chunk_size, int64_t ngroups,
+                                ssd_tensor *y, void *stream) {
+    if (!x || !Bm) return fail(SSD_ERR_INVALID_ARG, "x / B: null tensor descriptor");
+    if (x->ndim != 4 || Bm->ndim != 4) return fail(SSD_ERR_INVALID_ARG, "x / B: ndim must be 4");
+    const int64_t Bn = x->shape[0], L = x->shape[1], H = x->shape[2], P = x->shape[3];
+    const int64_t N = Bm->shape[3], Gn = ngroups, Q = chunk_size;
+    ssd_status st = check_geometry(Bn, L, H, P, N, Gn, Q);
+    if (st != SSD_OK) return st;
+    const int64_t nc = (L + Q - 1) / Q;
+    const int xdt = x->dtype;
+    const int64_t sx[4] = {Bn, L, H, P}, sdt[3] = {Bn, L, H}, sbc[4] = {Bn, L, Gn, N},
+                  sg[3] = {Bn, H, nc * Q}, ss[5] = {Bn, nc, H, P, N}, sh[1] = {H};
+    if ((st = check_tensor(x, "x", 4, sx, -1, false, true))) return st;
+    if ((st = check_tensor(dt, "dt", 3, sdt, SSD_F32, false, false))) return st;
+    if ((st = check_tensor(G, "G", 3, sg, SSD_F32, true, false))) return st;
+    if ((st = check_tensor(Bm, "B", 4, sbc, xdt, false, true))) return st;
+    if ((st = check_tensor(Cm, "C", 4, sbc, xdt, false, true))) return st;
+    if (D && (st = check_tensor(D, "D", 1, sh, SSD_F32, true, false))) return st;
+    if ((st = check_tensor(h_prev, "h_prev", 5, ss, xdt, true, true))) return st;
+    if ((st = check_tensor(y, "y", 4, sx, xdt, false, true))) return st;
+    const Range ry = range_of(y);
+    const Range ins[] = {range_of(x), range_of(dt), range_of(G), range_of(Bm),
+                         range_of(Cm), range_of(D), range_of(h_prev)};
+    for (const Range &r : ins)
+        if (overlap(ry, r)) return fail(SSD_ERR_INVALID_ARG, "y overlaps an input");
+    if (Bn == 0 || L == 0) return ok();
+    if ((st = check_device_ptrs({{x->data, "x"}, {dt->data, "dt"}, {G->data, "G"},
+                                 {Bm->data, "B"}, {Cm->data, "C"}, {D ? D->data : nullptr, "D"},
+                                 {h_prev->data, "h_prev"}, {y->data, "y"}})))
+        return st;
+    ssd::Args a;
+    a.d = ssd::Dims{Bn, L, H, P, N, Gn, Q, nc};
+    a.xdt = xdt;
+    fill_x(a, x);
+    fill_dt(a, dt);
+    a.G = static_cast<float *>(G->data);
+    fill_bc(a, Bm, Cm);
+    a.D = D ? static_cast<const float *>(D->data) : nullptr;
+    a.h_prev = h_prev->data;
+    a.hprev_dt = xdt;
+    fill_y(a, y);
+    if ((st = cuda_status(ssd::launch_chunk_scan(a, static_cast<cudaStream_t>(stream)),
+                          "chunk_scan")))
+        return st;
+    return ok();
+}
+
+}  // extern "C"

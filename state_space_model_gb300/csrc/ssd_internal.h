@@ -1,0 +1,51 @@
+// Internal problem description passed from the host API layer to the kernel
+// launchers.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime_api.h>
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define SSD_HD __host__ __device__
+#else
+#define SSD_HD
+#endif
+
+namespace ssd {
+
+enum : int { DT_F32 = 0, DT_BF16 = 1 };
+
+struct Dims {
+    int64_t B, L, H, P, N, G, Q, nc;
+    SSD_HD int64_t hpg() const { return H / G; }    // heads per group
+    SSD_HD int64_t Lp() const { return nc * Q; }    // zero-padded sequence length
+};
+
+// Every pointer is a device pointer.  Strides are in elements; the innermost
+// stride of every tensor is 1.  G, S, h_prev, h0 and final are contiguous.
+struct Args {
+    Dims d{};
+    int xdt = DT_BF16;                        // dtype of x, B, C, y
+    const void *x = nullptr;   int64_t x_sb = 0, x_sl = 0, x_sh = 0;
+    const float *dt = nullptr; int64_t dt_sb = 0, dt_sl = 0;
+    const float *A = nullptr;
+    const float *D = nullptr;                 // may be null (= 0)
+    const void *Bm = nullptr;  int64_t b_sb = 0, b_sl = 0, b_sg = 0;
+    const void *Cm = nullptr;  int64_t c_sb = 0, c_sl = 0, c_sg = 0;
+    const float *h0 = nullptr;                // may be null (= 0)
+    void *y = nullptr;         int64_t y_sb = 0, y_sl = 0, y_sh = 0;
+    float *final_states = nullptr;            // may be null (skip)
+    float *G = nullptr;                       // [B, H, nc*Q]
+    float *S = nullptr;                       // [B, nc, H, P, N]
+    void *h_prev = nullptr;                   // [B, nc, H, P, N]
+    int hprev_dt = DT_F32;
+};
+
+// Kernel launchers (one per step).  Each picks its kernel variant for the
+// geometry and dtype, launches on `stream` and returns the launch status.
+cudaError_t launch_chunk_cumsum(const Args &a, cudaStream_t stream);
+cudaError_t launch_chunk_state(const Args &a, cudaStream_t stream);
+cudaError_t launch_state_passing(const Args &a, cudaStream_t stream);
+cudaError_t launch_chunk_scan(const Args &a, cudaStream_t stream);
+
+}  // namespace ssd

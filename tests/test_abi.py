@@ -1,0 +1,203 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/*.h declares, and its host-side argument checks return the right
+status (and a detail naming the failed check) before any CUDA call.
+
+The descriptors here point at fake, aligned addresses: each case fails a
+pure-host check first, so nothing ever dereferences them.
+"""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+from state_space_model_gb300 import _native
+from state_space_model_gb300._native import SsdTensor
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+F32, BF16 = 0, 1
+FAKE = 0x7F0000000000  # 256-byte aligned, never dereferenced
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        names |= set(re.findall(r"\b(ssd_[A-Za-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from state_space_model_gb300 import build
+    build.build()
+    return _native.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert "ssd_chunked_fwd" in names and len(names) >= 8
+    out = subprocess.run(["nm", "-D", "--defined-only", _native.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(\w+)", out))
+    for n in names:
+        assert n in exported, f"{n} declared in include/ but not exported"
+        assert hasattr(lib, n)
+
+
+def test_status_strings(lib):
+    for code, name in _native.STATUS.items():
+        assert lib.ssd_status_string(code).decode() == name
+
+
+def tens(shape, dtype=BF16, strides=None, ptr=FAKE):
+    d = SsdTensor()
+    d.data = ptr
+    d.dtype = dtype
+    d.ndim = len(shape)
+    if strides is None:
+        strides, acc = [], 1
+        for s in reversed(shape):
+            strides.insert(0, acc)
+            acc *= s
+    for i, (s, st) in enumerate(zip(shape, strides)):
+        d.shape[i] = s
+        d.stride[i] = st
+    return d
+
+
+class Case:
+    """A valid bf16 problem of fake device tensors at distinct addresses."""
+
+    def __init__(self, B=2, L=300, H=4, P=64, N=128, G=2, Q=128, xdt=BF16):
+        self.B, self.L, self.H, self.P, self.N, self.G, self.Q = B, L, H, P, N, G, Q
+        base = [FAKE]
+
+        def nxt(nbytes):
+            p = base[0]
+            base[0] += (nbytes + 4095) // 4096 * 4096 + 4096
+            return p
+
+        es = 2 if xdt == BF16 else 4
+        self.x = tens((B, L, H, P), xdt, ptr=nxt(B * L * H * P * es))
+        self.dt = tens((B, L, H), F32, ptr=nxt(B * L * H * 4))
+        self.A = tens((H,), F32, ptr=nxt(H * 4))
+        self.Bm = tens((B, L, G, N), xdt, ptr=nxt(B * L * G * N * es))
+        self.Cm = tens((B, L, G, N), xdt, ptr=nxt(B * L * G * N * es))
+        self.D = tens((H,), F32, ptr=nxt(H * 4))
+        self.h0 = tens((B, H, P, N), F32, ptr=nxt(B * H * P * N * 4))
+        self.y = tens((B, L, H, P), xdt, ptr=nxt(B * L * H * P * es))
+        self.fin = tens((B, H, P, N), F32, ptr=nxt(B * H * P * N * 4))
+        self.ws_bytes = 1 << 40
+        self.ws = nxt(1 << 20) + (1 << 41)
+
+    def call(self, lib, **over):
+        a = dict(x=self.x, dt=self.dt, A=self.A, Bm=self.Bm, Cm=self.Cm, D=self.D,
+                 h0=self.h0, y=self.y, fin=self.fin, Q=self.Q, G=self.G,
+                 ws=self.ws, ws_bytes=self.ws_bytes)
+        a.update(over)
+        p = lambda t: None if t is None else ctypes.pointer(t)
+        return lib.ssd_chunked_fwd(p(a["x"]), p(a["dt"]), p(a["A"]), p(a["Bm"]), p(a["Cm"]),
+                                   p(a["D"]), p(a["h0"]), a["Q"], a["G"], p(a["y"]),
+                                   p(a["fin"]), a["ws"], a["ws_bytes"], None)
+
+
+def detail(lib):
+    return lib.ssd_last_error_detail().decode()
+
+
+def test_workspace_size(lib):
+    out = ctypes.c_size_t()
+    assert lib.ssd_workspace_size(8, 4096, 80, 64, 128, 1, 256, BF16, ctypes.byref(out)) == 0
+    B, L, H, P, N, Q = 8, 4096, 80, 64, 128, 256
+    nc = L // Q
+    need = B * H * nc * Q * 4 + B * nc * H * P * N * 4 + B * nc * H * P * N * 2
+    assert need <= out.value < need + 3 * 256
+    assert lib.ssd_workspace_size(1, 10, 3, 64, 128, 2, 256, BF16, ctypes.byref(out)) == 1
+    assert "multiple of ngroups" in detail(lib)
+    assert lib.ssd_workspace_size(1, 10, 4, 64, 128, 2, 100, BF16, ctypes.byref(out)) == 2
+    assert lib.ssd_workspace_size(1, 10, 4, 48, 128, 2, 128, BF16, ctypes.byref(out)) == 2
+    assert lib.ssd_workspace_size(1, 10, 4, 64, 128, 2, 128, 7, ctypes.byref(out)) == 1
+
+
+def test_error_paths(lib):
+    c = Case()
+    # null required descriptor
+    assert c.call(lib, x=None) == 1 and "x" in detail(lib)
+    assert c.call(lib, dt=None) == 1 and "dt" in detail(lib)
+    assert c.call(lib, y=None) == 1 and "y" in detail(lib)
+    # wrong dtype
+    assert c.call(lib, dt=tens((2, 300, 4), BF16, ptr=c.dt.data)) == 1
+    assert "dt" in detail(lib) and "dtype" in detail(lib)
+    assert c.call(lib, Bm=tens((2, 300, 2, 128), F32, ptr=c.Bm.data)) == 1
+    assert c.call(lib, x=tens((2, 300, 4, 64), 5, ptr=c.x.data)) == 1
+    # wrong shapes
+    assert c.call(lib, dt=tens((2, 299, 4), F32, ptr=c.dt.data)) == 1
+    assert "shape" in detail(lib)
+    assert c.call(lib, y=tens((2, 300, 4, 32), BF16, ptr=c.y.data)) == 1
+    assert c.call(lib, A=tens((5,), F32, ptr=c.A.data)) == 1
+    # heads not a multiple of groups, unsupported geometry
+    assert c.call(lib, G=3) == 1 and "ngroups" in detail(lib)
+    assert c.call(lib, Q=96) == 2 and "chunk_size" in detail(lib)
+    assert c.call(lib, Q=0) == 1
+    c2 = Case(P=48)
+    assert c2.call(lib) == 2 and "headdim" in detail(lib)
+    c3 = Case(N=256)
+    assert c3.call(lib) == 2 and "dstate" in detail(lib)
+    # innermost stride
+    assert c.call(lib, x=tens((2, 300, 4, 64), BF16, strides=(300 * 512, 512, 128, 2),
+                              ptr=c.x.data)) == 1
+    assert "innermost" in detail(lib)
+    # alignment of base pointer and of outer strides
+    assert c.call(lib, x=tens((2, 300, 4, 64), BF16, ptr=c.x.data + 2)) == 3
+    assert c.call(lib, x=tens((2, 300, 4, 64), BF16, strides=(300 * 4 * 68, 4 * 68, 68, 1),
+                              ptr=c.x.data)) == 3
+    assert "16 bytes" in detail(lib)
+    # non-contiguous states
+    assert c.call(lib, h0=tens((2, 4, 64, 128), F32, strides=(4 * 64 * 256, 64 * 256, 256, 1),
+                               ptr=c.h0.data)) == 1
+    # workspace
+    assert c.call(lib, ws_bytes=1000) == 4 and "workspace" in detail(lib)
+    assert c.call(lib, ws=None) == 4
+    assert c.call(lib, ws=c.ws + 16) == 3
+    # aliasing: y on top of x, final on top of initial_states
+    assert c.call(lib, y=tens((2, 300, 4, 64), BF16, ptr=c.x.data)) == 1
+    assert "overlaps" in detail(lib)
+    assert c.call(lib, fin=tens((2, 4, 64, 128), F32, ptr=c.h0.data)) == 1
+    # an empty batch is valid and launches nothing
+    e = Case(B=0)
+    assert e.call(lib) == 0 and detail(lib) == ""
+
+
+def test_stage_error_paths(lib):
+    c = Case()
+    p = ctypes.pointer
+    nc = -(-c.L // c.Q)
+    G = tens((2, 4, nc * c.Q), F32, ptr=c.ws)
+    assert lib.ssd_stage_chunk_cumsum(p(c.dt), p(c.A), 100, p(G), None) == 2
+    badG = tens((2, 4, c.L), F32, ptr=c.ws)
+    assert lib.ssd_stage_chunk_cumsum(p(c.dt), p(c.A), c.Q, p(badG), None) == 1
+    S = tens((2, nc, 4, 64, 128), F32, ptr=c.ws + (1 << 30))
+    assert lib.ssd_stage_chunk_state(p(c.x), p(c.Bm), p(c.dt), p(G), c.Q, 3, p(S), None) == 1
+    badS = tens((2, nc + 1, 4, 64, 128), F32, ptr=c.ws + (1 << 30))
+    assert lib.ssd_stage_chunk_state(p(c.x), p(c.Bm), p(c.dt), p(G), c.Q, 2, p(badS), None) == 1
+    hp = tens((2, nc, 4, 64, 128), BF16, ptr=c.ws + (1 << 31))
+    assert lib.ssd_stage_state_passing(p(S), p(G), p(c.h0), c.Q, p(hp), p(c.h0), None) == 1
+    assert "overlaps" in detail(lib)
+    hp32 = tens((2, nc, 4, 64, 128), F32, ptr=c.ws + (1 << 31))
+    assert lib.ssd_stage_chunk_scan(p(c.x), p(c.dt), p(G), p(c.Bm), p(c.Cm), p(c.D), p(hp32),
+                                    c.Q, 2, p(c.y), None) == 1
+    assert "h_prev" in detail(lib)
+
+
+def test_python_binding_rejects_cpu_tensors(lib):
+    import torch
+    from state_space_model_gb300 import ssd
+    x = torch.zeros(1, 64, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ssd.chunked_fwd(x, torch.zeros(1, 64, 2), torch.zeros(2), torch.zeros(1, 64, 1, 128),
+                        torch.zeros(1, 64, 1, 128), chunk_size=64)
