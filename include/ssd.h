@@ -108,6 +108,36 @@ ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt,
                            void *workspace, size_t workspace_bytes,
                            void *stream);
 
+/* ---- allocation-free variant ------------------------------------------------
+ * The pages have no counterpart of this call; it exists for callers that
+ * cannot hand the library a device workspace: code that runs where no
+ * allocator is reachable (a plug-in inside a host program that owns all
+ * device memory and exposes no workspace hook), or where calling cudaMalloc
+ * is not acceptable (it may synchronise the device and its latency is
+ * unbounded, which a fixed-latency loop cannot afford).
+ *
+ * Same inputs, outputs and results as ssd_chunked_fwd, but its scratch comes
+ * from one file-scope __device__ array of SSD_STATIC_SCRATCH_BYTES that every
+ * GPU loading this library holds until the process exits.  The call
+ * allocates and frees nothing.  Problems whose scratch (ssd_workspace_size)
+ * exceeds SSD_STATIC_SCRATCH_BYTES are rejected with SSD_ERR_WORKSPACE before
+ * any launch.  The first call on a device (with that device current) looks
+ * up the array's device address and caches it; make that first call before
+ * any stream capture.  All calls on a device share the one array, which
+ * keeps the last call's contents (nothing in it needs to start at zero:
+ * every byte a call reads is written earlier in that call), so calls whose
+ * execution overlaps on the GPU (different streams, no ordering) race and
+ * corrupt each other's results: order them on one stream or with events. */
+#define SSD_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+
+ssd_status ssd_chunked_fwd_static_scratch(const ssd_tensor *x, const ssd_tensor *dt,
+                                          const ssd_tensor *A, const ssd_tensor *B,
+                                          const ssd_tensor *C, const ssd_tensor *D,
+                                          const ssd_tensor *initial_states,
+                                          int64_t chunk_size, int64_t ngroups,
+                                          ssd_tensor *y, ssd_tensor *final_states,
+                                          void *stream);
+
 /* ---- stage entry points (the four steps of ssd_chunked_fwd, one call each;
  *      same conventions; used to check each step on its own) ---------------- */
 

@@ -225,6 +225,17 @@ void fill_y(ssd::Args &a, ssd_tensor *y) {
 
 }  // namespace
 
+namespace ssd {
+void set_error_detail(const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_detail = buf;
+}
+}  // namespace ssd
+
 extern "C" {
 
 const char *ssd_status_string(ssd_status s) {

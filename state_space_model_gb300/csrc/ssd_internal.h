@@ -41,6 +41,9 @@ struct Args {
     int hprev_dt = DT_F32;
 };
 
+// Records the text ssd_last_error_detail() returns on this thread.
+void set_error_detail(const char *fmt, ...);
+
 // Kernel launchers (one per step).  Each picks its kernel variant for the
 // geometry and dtype, launches on `stream` and returns the launch status.
 cudaError_t launch_chunk_cumsum(const Args &a, cudaStream_t stream);

@@ -89,6 +89,28 @@ def chunked_fwd(x, dt, A, B, C, D=None, initial_states=None, chunk_size=256, ngr
     return y, final_states
 
 
+def chunked_fwd_static_scratch(x, dt, A, B, C, D=None, initial_states=None, chunk_size=256,
+                               ngroups=1, *, return_final_states=True, y=None,
+                               final_states=None):
+    """The SSD forward without any workspace argument: the library takes its
+    scratch from a fixed device array of SSD_STATIC_SCRATCH_BYTES (for callers
+    that cannot allocate device memory).  Problems needing more scratch than
+    that raise SsdError(SSD_ERR_WORKSPACE).  Calls that overlap on the GPU
+    share that array and race; order them on one stream."""
+    dev = _device_of(x, dt, A, B, C, D, initial_states, y, final_states)
+    Bn, L, H, P = x.shape
+    N = B.shape[-1]
+    if y is None:
+        y = torch.empty((Bn, L, H, P), dtype=x.dtype, device=dev)
+    if final_states is None and return_final_states:
+        final_states = torch.empty((Bn, H, P, N), dtype=torch.float32, device=dev)
+    st = _native.load().ssd_chunked_fwd_static_scratch(
+        _desc(x), _desc(dt), _desc(A), _desc(B), _desc(C), _desc(D), _desc(initial_states),
+        chunk_size, ngroups, _desc(y), _desc(final_states), _stream(dev))
+    _native.check(st, "ssd_chunked_fwd_static_scratch")
+    return y, final_states
+
+
 # ---- the four steps, one call each -----------------------------------------
 
 def chunk_cumsum(dt, A, chunk_size, out=None):
