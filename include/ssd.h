@@ -81,6 +81,13 @@ const char *ssd_status_string(ssd_status status);
  * valid until the next call on that thread); "" after a successful call. */
 const char *ssd_last_error_detail(void);
 
+/* Waits for `stream`, then reports (and clears) the device-side error word of
+ * the current device: SSD_ERR_TIMEOUT if any kernel of this library gave up a
+ * bounded wait since the last call (its outputs are then not valid), SSD_OK
+ * otherwise, SSD_ERR_CUDA if CUDA itself reports an error.  This is the only
+ * entry point that synchronises; call it where a check is wanted. */
+ssd_status ssd_device_status(void *stream);
+
 /* Bytes of device workspace ssd_chunked_fwd needs for this problem, written
  * to *bytes.  x_dtype is the ssd_dtype of x, B, C.  The workspace holds the
  * scaled in-chunk cumulative sums G [B, H, nc*Q] f32, the per-chunk states

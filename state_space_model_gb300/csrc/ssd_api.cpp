@@ -4,6 +4,7 @@
 // frees or synchronises.
 #include "ssd.h"
 #include "ssd_internal.h"
+#include "ssd_tc.cuh"
 
 #include <cstdarg>
 #include <cstdio>
@@ -252,6 +253,27 @@ const char *ssd_status_string(ssd_status s) {
 }
 
 const char *ssd_last_error_detail(void) { return g_detail.c_str(); }
+
+ssd_status ssd_device_status(void *stream) {
+    unsigned int *word = nullptr;
+    ssd_status st;
+    if ((st = cuda_status(ssd::device_error_word(&word), "device error word"))) return st;
+    if ((st = cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)),
+                          "stream synchronize")))
+        return st;
+    unsigned int v = 0;
+    if ((st = cuda_status(cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost), "read")))
+        return st;
+    if (v) {
+        const unsigned int zero = 0;
+        if ((st = cuda_status(cudaMemcpy(word, &zero, sizeof zero, cudaMemcpyHostToDevice),
+                              "clear")))
+            return st;
+        return fail(SSD_ERR_TIMEOUT, "a kernel gave up a bounded wait (flags 0x%x); outputs of "
+                    "the calls since the last check are not valid", v);
+    }
+    return ok();
+}
 
 ssd_status ssd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
                               int64_t dstate, int64_t ngroups, int64_t chunk_size,

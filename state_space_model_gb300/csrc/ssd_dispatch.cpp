@@ -1,14 +1,39 @@
-// Picks the kernel variant of each step for the problem's dtype and geometry.
+// Picks the kernel variant of each step for the problem's dtype and geometry:
+// the tensor-core kernels for bf16 inputs with P = 64, N = 128 (and Q of 128
+// or 256 for chunk_scan), the CUDA-core kernels for everything else.
 #include "ssd_internal.h"
 #include "ssd_simt.cuh"
+#include "ssd_tc.cuh"
+
+#include <cstdlib>
 
 namespace ssd {
+namespace {
+// SSD_FORCE_SIMT=1 selects the CUDA-core variants for every shape (for
+// comparisons only; read once per process).
+bool force_simt() {
+    static const bool v = [] {
+        const char *e = std::getenv("SSD_FORCE_SIMT");
+        return e && e[0] == '1';
+    }();
+    return v;
+}
+}  // namespace
 
 cudaError_t launch_chunk_cumsum(const Args &a, cudaStream_t s) { return simt_chunk_cumsum(a, s); }
-cudaError_t launch_chunk_state(const Args &a, cudaStream_t s) { return simt_chunk_state(a, s); }
+
+cudaError_t launch_chunk_state(const Args &a, cudaStream_t s) {
+    if (!force_simt() && tc_chunk_state_supported(a)) return tc_chunk_state(a, s);
+    return simt_chunk_state(a, s);
+}
+
 cudaError_t launch_state_passing(const Args &a, cudaStream_t s) {
     return simt_state_passing(a, s);
 }
-cudaError_t launch_chunk_scan(const Args &a, cudaStream_t s) { return simt_chunk_scan(a, s); }
+
+cudaError_t launch_chunk_scan(const Args &a, cudaStream_t s) {
+    if (!force_simt() && tc_chunk_scan_supported(a)) return tc_chunk_scan(a, s);
+    return simt_chunk_scan(a, s);
+}
 
 }  // namespace ssd

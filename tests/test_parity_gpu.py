@@ -47,11 +47,21 @@ def to_dev(inp):
     return {k: (None if v is None else v.cuda()) for k, v in inp.items()}
 
 
+def device_ok():
+    """No kernel gave up a bounded wait since the last check."""
+    import ctypes
+    from state_space_model_gb300 import _native
+    lib = _native.load()
+    st = lib.ssd_device_status(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, lib.ssd_last_error_detail().decode()
+
+
 def run(w, inp, **kw):
     d = to_dev(inp)
     y, f = ssd().chunked_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"],
                              d["initial_states"], w.chunk_size, w.ngroups, **kw)
     torch.cuda.synchronize()
+    device_ok()
     return y.float().cpu().double().numpy(), (None if f is None else f.cpu().double().numpy())
 
 
