@@ -340,32 +340,47 @@ def main():
     tokens = B * L
     value = world * tokens / (ms / 1e3)
 
-    # per-step kernel durations: the four stage entry points, events between them
-    nc = -(-L // w.chunk_size)
-    G = torch.empty((B, H, nc * w.chunk_size), dtype=torch.float32, device=dev)
-    S = torch.empty((B, nc, H, P, N), dtype=torch.float32, device=dev)
-    hp = torch.empty((B, nc, H, P, N), dtype=w.torch_dtype, device=dev)
-    kstats = {k: 0.0 for k in ("chunk_cumsum", "chunk_state", "state_passing", "chunk_scan")}
+    plan = ssd.describe_plan(B, L, H, P, N, w.ngroups, w.chunk_size, w.torch_dtype)
+    fused = plan.startswith("fused")
     reps = max(10, min(args.steps, 200))
-    for it in range(reps + 3):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-        evs[0].record(stream)
-        ssd.chunk_cumsum(d["dt"], d["A"], w.chunk_size, out=G)
-        evs[1].record(stream)
-        ssd.chunk_state(d["x"], d["B"], d["dt"], G, w.chunk_size, w.ngroups, out=S)
-        evs[2].record(stream)
-        ssd.state_passing(S, G, d["initial_states"], w.chunk_size, out=(hp, fin))
-        evs[3].record(stream)
-        ssd.chunk_scan(d["x"], d["dt"], G, d["B"], d["C"], d["D"], hp, w.chunk_size, w.ngroups,
-                       out=y)
-        evs[4].record(stream)
-        torch.cuda.synchronize()
-        if it >= 3:
-            for i, k in enumerate(kstats):
-                kstats[k] += evs[i].elapsed_time(evs[i + 1]) / reps
+    sb = stage_bytes(w)
+    if fused:
+        # one kernel per step: its launches timed one by one with events around each
+        kstats = {"ssd_fused": 0.0}
+        sb["ssd_fused"] = path_work(w)[0]
+        for it in range(reps + 3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if it >= 3:
+                kstats["ssd_fused"] += e0.elapsed_time(e1) / reps
+    else:
+        # the four stage entry points, events between them
+        nc = -(-L // w.chunk_size)
+        G = torch.empty((B, H, nc * w.chunk_size), dtype=torch.float32, device=dev)
+        S = torch.empty((B, nc, H, P, N), dtype=torch.float32, device=dev)
+        hp = torch.empty((B, nc, H, P, N), dtype=w.torch_dtype, device=dev)
+        kstats = {k: 0.0 for k in ("chunk_cumsum", "chunk_state", "state_passing", "chunk_scan")}
+        for it in range(reps + 3):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            evs[0].record(stream)
+            ssd.chunk_cumsum(d["dt"], d["A"], w.chunk_size, out=G)
+            evs[1].record(stream)
+            ssd.chunk_state(d["x"], d["B"], d["dt"], G, w.chunk_size, w.ngroups, out=S)
+            evs[2].record(stream)
+            ssd.state_passing(S, G, d["initial_states"], w.chunk_size, out=(hp, fin))
+            evs[3].record(stream)
+            ssd.chunk_scan(d["x"], d["dt"], G, d["B"], d["C"], d["D"], hp, w.chunk_size,
+                           w.ngroups, out=y)
+            evs[4].record(stream)
+            torch.cuda.synchronize()
+            if it >= 3:
+                for i, k in enumerate(kstats):
+                    kstats[k] += evs[i].elapsed_time(evs[i + 1]) / reps
     dom = max(kstats, key=kstats.get)
     pk = peaks()
-    sb = stage_bytes(w)
     achieved = sb[dom] / (kstats[dom] / 1e3) / 1e9
     traffic = recorded_traffic(dom, w.name)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"],
@@ -431,7 +446,7 @@ def main():
                               f"{L2_BYTES / 1e6:.0f} MB), no flush")
                        if in_bytes > L2_BYTES else "inputs smaller than L2"},
             "roofline": roofline, "path_roofline": path_roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 4 * args.steps, "clocks": clk,
+            "gpu_launches": (1 if fused else 4) * args.steps, "plan": plan, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -99,6 +99,14 @@ ssd_status ssd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads,
                               int64_t chunk_size, int32_t x_dtype,
                               size_t *bytes);
 
+/* One line naming the kernels ssd_chunked_fwd would launch for this problem
+ * ("fused: ..." for the single-kernel path, "staged: ..." for the four-step
+ * path), or the reason it would be rejected.  Thread-local storage, valid
+ * until the next call on the thread.  Never launches or touches the GPU. */
+const char *ssd_describe_plan(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                              int64_t dstate, int64_t ngroups, int64_t chunk_size,
+                              int32_t x_dtype);
+
 /* The SSD chunked forward: y and (optionally) final_states from x, dt, A, B,
  * C, D, initial_states, as defined at the top of this file.  A sequence
  * length that is not a multiple of chunk_size is handled as if zero-padded

@@ -70,6 +70,8 @@ def load():
             lib.ssd_status_string.restype = ctypes.c_char_p
             lib.ssd_last_error_detail.argtypes = []
             lib.ssd_last_error_detail.restype = ctypes.c_char_p
+            lib.ssd_describe_plan.argtypes = [_I64] * 7 + [_I32]
+            lib.ssd_describe_plan.restype = ctypes.c_char_p
             _lib = lib
     return _lib
 

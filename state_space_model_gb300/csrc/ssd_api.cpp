@@ -140,12 +140,17 @@ ssd_status check_geometry(int64_t B, int64_t L, int64_t H, int64_t P, int64_t N,
     return SSD_OK;
 }
 
+// Either the fused single-kernel path (no workspace) or the four-step path
+// with its intermediates in the workspace.
 struct Plan {
+    bool fused;
     size_t off_G, off_S, off_hp, total;
 };
 
 Plan plan_workspace(const ssd::Dims &d, int xdt) {
     Plan p{};
+    p.fused = ssd::use_fused(d, xdt);
+    if (p.fused) return p;
     const size_t g = size_t(d.B) * d.H * d.nc * d.Q * 4;
     const size_t s = size_t(d.B) * d.nc * d.H * d.P * d.N * 4;
     const size_t hp = size_t(d.B) * d.nc * d.H * d.P * d.N * elem_size(xdt);
@@ -254,6 +259,42 @@ const char *ssd_status_string(ssd_status s) {
 
 const char *ssd_last_error_detail(void) { return g_detail.c_str(); }
 
+const char *ssd_describe_plan(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                              int64_t dstate, int64_t ngroups, int64_t chunk_size,
+                              int32_t x_dtype) {
+    thread_local std::string text;
+    if (x_dtype != SSD_F32 && x_dtype != SSD_BF16) {
+        text = "rejected: unknown dtype code";
+        return text.c_str();
+    }
+    const std::string saved = g_detail;
+    if (check_geometry(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size) != SSD_OK) {
+        text = "rejected: " + g_detail;
+        g_detail = saved;
+        return text.c_str();
+    }
+    ssd::Dims d{batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size,
+                (seqlen + chunk_size - 1) / chunk_size};
+    ssd::Args a;
+    a.d = d;
+    a.xdt = x_dtype;
+    a.hprev_dt = x_dtype;
+    char buf[256];
+    if (ssd::use_fused(d, x_dtype)) {
+        snprintf(buf, sizeof buf,
+                 "fused: k_ssd_fused x %lld CTAs ((batch, head) slabs), 128-token blocks, "
+                 "tcgen05 + TMA, no workspace",
+                 (long long)(batch * nheads));
+    } else {
+        snprintf(buf, sizeof buf,
+                 "staged: chunk_cumsum simt, chunk_state %s, state_passing simt, chunk_scan %s",
+                 ssd::uses_tc_chunk_state(a) ? "tcgen05" : "simt",
+                 ssd::uses_tc_chunk_scan(a) ? "tcgen05" : "simt");
+    }
+    text = buf;
+    return text.c_str();
+}
+
 ssd_status ssd_device_status(void *stream) {
     unsigned int *word = nullptr;
     ssd_status st;
@@ -320,7 +361,7 @@ ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt, const ssd_
 
     ssd::Dims d{Bn, L, H, P, N, G, Q, (L + Q - 1) / Q};
     const Plan plan = plan_workspace(d, xdt);
-    if (Bn > 0) {
+    if (Bn > 0 && plan.total > 0) {
         if (workspace_bytes < plan.total)
             return fail(SSD_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes,
                         plan.total);
@@ -370,6 +411,10 @@ ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt, const ssd_
     a.hprev_dt = xdt;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (plan.fused) {
+        if ((st = cuda_status(ssd::launch_fused(a, s), "fused forward"))) return st;
+        return ok();
+    }
     if (L > 0) {
         if ((st = cuda_status(ssd::launch_chunk_cumsum(a, s), "chunk_cumsum"))) return st;
         if ((st = cuda_status(ssd::launch_chunk_state(a, s), "chunk_state"))) return st;

@@ -20,6 +20,21 @@ bool force_simt() {
 }
 }  // namespace
 
+// SSD_FORCE_STAGED=1 makes ssd_chunked_fwd run the four separate steps even
+// where the fused kernel applies (for comparisons only).
+bool use_fused(const Dims &d, int xdt) {
+    static const bool staged = [] {
+        const char *e = std::getenv("SSD_FORCE_STAGED");
+        return e && e[0] == '1';
+    }();
+    // an empty sequence has nothing to tile (a TMA map cannot have a zero
+    // extent); the four-step path then just copies the initial state
+    return !staged && !force_simt() && d.L > 0 && fused_supported(d, xdt);
+}
+
+bool uses_tc_chunk_state(const Args &a) { return !force_simt() && tc_chunk_state_supported(a); }
+bool uses_tc_chunk_scan(const Args &a) { return !force_simt() && tc_chunk_scan_supported(a); }
+
 cudaError_t launch_chunk_cumsum(const Args &a, cudaStream_t s) { return simt_chunk_cumsum(a, s); }
 
 cudaError_t launch_chunk_state(const Args &a, cudaStream_t s) {

@@ -44,6 +44,12 @@ struct Args {
 // Records the text ssd_last_error_detail() returns on this thread.
 void set_error_detail(const char *fmt, ...);
 
+// True when ssd_chunked_fwd runs the fused single-kernel path for this problem.
+bool use_fused(const Dims &d, int xdt);
+// Which variant the four-step path picks for chunk_state / chunk_scan.
+bool uses_tc_chunk_state(const Args &a);
+bool uses_tc_chunk_scan(const Args &a);
+
 // Kernel launchers (one per step).  Each picks its kernel variant for the
 // geometry and dtype, launches on `stream` and returns the launch status.
 cudaError_t launch_chunk_cumsum(const Args &a, cudaStream_t stream);

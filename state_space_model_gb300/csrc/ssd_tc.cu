@@ -13,11 +13,11 @@
 #include "ptx_sm100.cuh"
 #include "ssd_internal.h"
 #include "ssd_tc.cuh"
+#include "ssd_tmap.h"
 
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
-#include <cudaTypedefs.h>
 
 #include <mutex>
 
@@ -498,49 +498,16 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 // host side
 
 std::mutex g_mu;
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 unsigned int *g_err_addr[256] = {};
 
-cudaError_t get_encode(PFN_cuTensorMapEncodeTiled_v12000 *out) {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_encode) {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                         cudaEnableDefault, &q);
-        if (e != cudaSuccess) return e;
-        if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
-        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-    *out = g_encode;
-    return cudaSuccess;
-}
-
-// bf16 4-D tensor map with a {64, 1, 64, 1} box and 128-byte swizzle.
-// dims/strides are innermost first; strides in bytes for dims 1..3.
 cudaError_t make_tmap_bf16_4d(CUtensorMap *m, const void *base, const uint64_t dims[4],
                               const uint64_t strides[3], const uint32_t box[4]) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc;
-    cudaError_t e = get_encode(&enc);
-    if (e != cudaSuccess) return e;
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    return make_tmap_bf16(m, base, 4, dims, strides, box);
 }
 
-// bf16 tensor map of rank 3 (innermost first) with 128-byte swizzle.
 cudaError_t make_tmap_bf16_3d(CUtensorMap *m, const void *base, const uint64_t dims[3],
                               const uint64_t strides[2], const uint32_t box[3]) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc;
-    cudaError_t e = get_encode(&enc);
-    if (e != cudaSuccess) return e;
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    return make_tmap_bf16(m, base, 3, dims, strides, box);
 }
 
 template <int QB>

@@ -66,6 +66,14 @@ def workspace_size(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size,
     return int(out.value)
 
 
+def describe_plan(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size,
+                  dtype=torch.bfloat16) -> str:
+    """Which kernels ssd_chunked_fwd launches for this problem ("fused: ..." or
+    "staged: ..."), or why it would be rejected."""
+    return _native.load().ssd_describe_plan(batch, seqlen, nheads, headdim, dstate, ngroups,
+                                            chunk_size, _DTYPES.get(dtype, 99)).decode()
+
+
 def chunked_fwd(x, dt, A, B, C, D=None, initial_states=None, chunk_size=256, ngroups=1, *,
                 return_final_states=True, y=None, final_states=None, workspace=None):
     """SSD chunked forward.  Returns ``(y, final_states)`` (the latter None when

@@ -73,7 +73,7 @@ def tens(shape, dtype=BF16, strides=None, ptr=FAKE):
 class Case:
     """A valid bf16 problem of fake device tensors at distinct addresses."""
 
-    def __init__(self, B=2, L=300, H=4, P=64, N=128, G=2, Q=128, xdt=BF16):
+    def __init__(self, B=2, L=300, H=4, P=64, N=128, G=2, Q=64, xdt=BF16):
         self.B, self.L, self.H, self.P, self.N, self.G, self.Q = B, L, H, P, N, G, Q
         base = [FAKE]
 
@@ -112,8 +112,12 @@ def detail(lib):
 
 def test_workspace_size(lib):
     out = ctypes.c_size_t()
+    # the fused single-kernel path needs no workspace
     assert lib.ssd_workspace_size(8, 4096, 80, 64, 128, 1, 256, BF16, ctypes.byref(out)) == 0
-    B, L, H, P, N, Q = 8, 4096, 80, 64, 128, 256
+    assert out.value == 0
+    # the four-step path keeps G, S and h_prev there
+    assert lib.ssd_workspace_size(8, 4096, 80, 64, 128, 1, 64, BF16, ctypes.byref(out)) == 0
+    B, L, H, P, N, Q = 8, 4096, 80, 64, 128, 64
     nc = L // Q
     need = B * H * nc * Q * 4 + B * nc * H * P * N * 4 + B * nc * H * P * N * 2
     assert need <= out.value < need + 3 * 256
@@ -122,6 +126,15 @@ def test_workspace_size(lib):
     assert lib.ssd_workspace_size(1, 10, 4, 64, 128, 2, 100, BF16, ctypes.byref(out)) == 2
     assert lib.ssd_workspace_size(1, 10, 4, 48, 128, 2, 128, BF16, ctypes.byref(out)) == 2
     assert lib.ssd_workspace_size(1, 10, 4, 64, 128, 2, 128, 7, ctypes.byref(out)) == 1
+
+
+def test_describe_plan(lib):
+    d = lambda *a: lib.ssd_describe_plan(*a).decode()
+    assert d(8, 4096, 80, 64, 128, 1, 256, BF16).startswith("fused")
+    assert d(1, 256, 4, 16, 16, 1, 64, F32).startswith("staged")
+    assert "tcgen05" in d(2, 300, 4, 64, 128, 1, 64, BF16)
+    assert d(1, 10, 4, 64, 128, 1, 100, BF16).startswith("rejected")
+    assert d(1, 10, 4, 64, 128, 1, 64, 9).startswith("rejected")
 
 
 def test_error_paths(lib):

@@ -189,6 +189,31 @@ def test_workload_parity(name):
         assert rel(fs[k], fr[k]) < TOL[w.dtype], f"final slab {slabs[k]}"
 
 
+@pytest.mark.parametrize("Q", [128, 256])
+def test_staged_path_composed_on_device(Q):
+    """The four step entry points chained on the GPU (the path ssd_chunked_fwd
+    takes where the fused kernel does not apply) against the recurrence."""
+    w = gen.small_case("bf16", batch=2, seqlen=700, nheads=4, ngroups=2, chunk_size=Q)
+    inp = gen.make_inputs(w)
+    d = to_dev(inp)
+    m = ssd()
+    G = m.chunk_cumsum(d["dt"], d["A"], Q)
+    S = m.chunk_state(d["x"], d["B"], d["dt"], G, Q, w.ngroups)
+    hp, fin = m.state_passing(S, G, d["initial_states"], Q, state_dtype=torch.bfloat16)
+    y = m.chunk_scan(d["x"], d["dt"], G, d["B"], d["C"], d["D"], hp, Q, w.ngroups)
+    torch.cuda.synchronize()
+    device_ok()
+    yr, fr = oracle_full(w, inp)
+    assert rel(y.float().cpu().numpy(), yr) < TOL["bf16"]
+    assert rel(fin.cpu().numpy(), fr) < TOL["bf16"]
+
+
+def test_plan_choice():
+    m = ssd()
+    assert m.describe_plan(8, 4096, 80, 64, 128, 1, 256).startswith("fused")
+    assert m.describe_plan(1, 256, 4, 16, 16, 1, 64, torch.float32).startswith("staged")
+
+
 # ---------------------------------------------------------------------------
 # edge cases
 

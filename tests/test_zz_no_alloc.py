@@ -39,7 +39,9 @@ def rel(a, b):
 def test_static_scratch_matches_workspace_entry_point(lib):
     from state_space_model_gb300 import ssd
     from state_space_model_gb300._native import SSD_BF16  # noqa: F401
-    w = gen.small_case("bf16", batch=2, seqlen=600, nheads=4, ngroups=2, chunk_size=128)
+    # a shape that runs the four-step path, which needs scratch memory
+    w = gen.small_case("bf16", batch=2, seqlen=600, nheads=4, ngroups=2, chunk_size=64)
+    assert ssd.workspace_size(2, 600, 4, 64, 128, 2, 64, torch.bfloat16) > 0
     inp = {k: (None if v is None else v.cuda()) for k, v in gen.make_inputs(w).items()}
     y_ref, f_ref = ssd.chunked_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
                                    inp["initial_states"], w.chunk_size, w.ngroups)
@@ -62,12 +64,12 @@ def test_static_scratch_rejects_problems_above_its_size(lib):
     from state_space_model_gb300 import ssd
     from state_space_model_gb300._native import SsdError
     B, L, H, P, N = 2, 8192, 32, 64, 128
-    need = ssd.workspace_size(B, L, H, P, N, 1, 256, torch.bfloat16)
+    need = ssd.workspace_size(B, L, H, P, N, 1, 64, torch.bfloat16)
     assert need > (64 << 20)
     x = torch.zeros(B, L, H, P, dtype=torch.bfloat16, device="cuda")
     dt = torch.zeros(B, L, H, device="cuda")
     A = torch.zeros(H, device="cuda")
     Bm = torch.zeros(B, L, 1, N, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(SsdError) as ei:
-        ssd.chunked_fwd_static_scratch(x, dt, A, Bm, Bm.clone(), chunk_size=256, ngroups=1)
+        ssd.chunked_fwd_static_scratch(x, dt, A, Bm, Bm.clone(), chunk_size=64, ngroups=1)
     assert ei.value.status == 4 and "static scratch" in ei.value.detail
