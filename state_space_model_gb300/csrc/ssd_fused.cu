@@ -23,13 +23,14 @@
 // entries by -inf before it is evaluated, so no positive exponent of the
 // decay is ever computed.
 //
-// Roles: warp 0 = TMA producer (128-byte swizzle, no multicast), warp 1 =
-// tensor-memory owner and MMA issuer, warps 2..5 = math (thread r owns tile
-// row / state row r = TMEM lane r).  Tensor memory (256 columns): [0,64) C B^T
-// then L, [64,128) C B^T then S^T, [128,192) inter, [192,256) intra.  Shared
-// memory (~99 KB, two CTAs per SM): the C, B and x tiles, and one buffer that
-// holds the bf16 carried state [n][p] (inter's operand) and then w o x [j][p]
-// (the state product's operand).
+// The blocks of one slab are software-pipelined across two stages: only the
+// fp32 state update h(k + 1) = 2^(g_end) h(k) + S(k) and the product C h^T it
+// feeds are serial; C B^T, L, L x and B^T (w o x) of later blocks proceed
+// while earlier blocks are drained.  Roles: warp 0 = TMA producer (128-byte
+// swizzle, no multicast), warp 1 = tensor-memory owner and MMA issuer, warps
+// 2..9 = warpgroup A (w o x and L), warps 10..13 = warpgroup B (state update,
+// y).  A thread owns tile row / state row r = its TMEM lane.  One CTA per SM
+// (512 TMEM columns, ~213 KB of shared memory).
 #include "ptx_sm100.cuh"
 #include "ssd_internal.h"
 #include "ssd_tc.cuh"
@@ -58,15 +59,22 @@ struct FusedParams {
     unsigned int *err;
 };
 
+// Shared memory (one CTA per SM): two stages of the C, B and x tiles and of
+// w o x, the bf16 carried-state operand, and per-stage small arrays.
 struct FusedSmem {
-    static constexpr int kC = 0;         // 2 x [128 tokens][128 B]  C, K-major (state)
-    static constexpr int kB = 32768;     // 2 x [128 tokens][128 B]  B, K-major (state)
-    static constexpr int kX = 65536;     // [128 tokens][128 B]      x, MN-major (headdim)
-    static constexpr int kXH = 81920;    // [128][128 B]: bf16 state [n][p] / w o x [j][p]
-    static constexpr int kF = 98304;     // ngd[128] (float), w2[128] (bf16x2), wsum[4]
-    static constexpr int kBar = kF + (2 * 128 + 4) * 4;
-    static constexpr int kBytes = kBar + 128 + 1024;
+    static constexpr int kC = 0;          // 2 stages x 2 x [128 tokens][128 B]  C, K-major
+    static constexpr int kB = 65536;      // 2 stages x 2 x [128 tokens][128 B]  B, K-major
+    static constexpr int kX = 131072;     // 2 stages x [128 tokens][128 B]      x, MN-major
+    static constexpr int kXP = 163840;    // 2 stages x [128 tokens][128 B]      w o x
+    static constexpr int kHB = 196608;    // [128 n][128 B]                      bf16 state
+    static constexpr int kF = 212992;     // grow, ngd, w2, vcol [2][128]; wsum, gpiv [2][4]
+    static constexpr int kBar = kF + (8 * 128 + 16) * 4;
+    static constexpr int kBytes = kBar + 256 + 1024;
 };
+
+constexpr int kThreads = 448;             // 14 warps
+constexpr int kWgA = 256;                 // warpgroup A threads (warps 2..9)
+
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -129,23 +137,83 @@ __device__ __forceinline__ void l_block(const uint32_t (&v)[32], int col0, bool 
     }
 }
 
-__global__ void __launch_bounds__(192, 2)
+// One 32-column block strictly below the diagonal block of row r: with p the
+// block's last row, 2^(g_r - g_j) dt_j = 2^(g_r - g_p) * (2^(g_p - g_j) dt_j),
+// both factors <= 1 (times dt), so the entries are cb[j] * u * vcol[j] with
+// u = 2^(g_r - g_p) and vcol[j] = 2^(g_p - g_j) dt_j: no exponent per entry.
+__device__ __forceinline__ void l_block_below(const uint32_t (&v)[32], int col0, float u,
+                                              const float *vcol, uint32_t (&out)[16]) {
+    const float2 u2 = make_float2(u, u);
+#pragma unroll
+    for (int jj = 0; jj < 32; jj += 4) {
+        const float4 c4 = *reinterpret_cast<const float4 *>(vcol + col0 + jj);
+        const float2 e0 = __fmul2_rn(
+            __fmul2_rn(make_float2(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1])),
+                       make_float2(c4.x, c4.y)),
+            u2);
+        const float2 e1 = __fmul2_rn(
+            __fmul2_rn(make_float2(__uint_as_float(v[jj + 2]), __uint_as_float(v[jj + 3])),
+                       make_float2(c4.z, c4.w)),
+            u2);
+        out[jj >> 1] = pack_bf16(e0.x, e0.y);
+        out[(jj >> 1) + 1] = pack_bf16(e1.x, e1.y);
+    }
+}
+
+// Block-local cumulative sum of A dt over the 128 rows owned by one math
+// warpgroup (thread r holds row r); returns g_r and g_end in log2 units.
+// `bar` is the warpgroup's named barrier, `wsum` its 4-float scratch.
+__device__ __forceinline__ void block_cumsum(float adt, int q, int lane, int bar, float *wsum,
+                                             float &gr, float &gend) {
+    float s = adt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, s, off);
+        if (lane >= off) s += o;
+    }
+    if (lane == 31) wsum[q] = s;
+    asm volatile("bar.sync %0, 128;" ::"r"(bar) : "memory");
+    float pre = 0.f;
+    for (int qq = 0; qq < q; ++qq) pre += wsum[qq];
+    const float tot = ((wsum[0] + wsum[1]) + wsum[2]) + wsum[3];
+    gr = (pre + s) * kLog2e;
+    gend = tot * kLog2e;
+}
+
+// Warps: 0 = TMA producer; 1 = tensor-memory owner and MMA issuer; 2..9 =
+// warpgroup A (w o x and the decay operand L; two warps per TMEM lane
+// quarter, splitting the column blocks); 10..13 = warpgroup B (state update
+// and y).  Block k uses stage s = k & 1 of every double buffer.  Tensor
+// memory: [128 s, +128) = C B^T of stage s, then L in its first 64 columns
+// and S^T in its last 64; [256 + 64 s, +64) = inter; [384 + 64 s, +64) = intra.
+//
+// Only the carried state is serial: h(k + 1) = 2^(g_end) h(k) + S(k), with S(k)
+// independent of h.  The MMA issuer therefore polls its three inputs -- the
+// state entering block k (for C h^T), the decay operand of block k (for L x
+// and S^T) and the operands of block k + 1 (for C B^T) -- and issues
+// whichever is ready, C h^T first.
+__global__ void __launch_bounds__(kThreads, 1)
 k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
-            const __grid_constant__ CUtensorMap tm_c, const FusedParams p) {
+            const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_y,
+            const FusedParams p) {
     using SM = FusedSmem;
-    constexpr uint32_t kCols = 256;
+    constexpr uint32_t kCols = 512;
     constexpr uint32_t kIdCB = ptx::idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t kIdKmn = ptx::idesc_bf16_f32(128, 64, false, true);   // A K-major, B MN-major
     constexpr uint32_t kIdState = ptx::idesc_bf16_f32(128, 64, true, true);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
-    float *ngd = reinterpret_cast<float *>(smem + SM::kF);
-    uint32_t *w2 = reinterpret_cast<uint32_t *>(ngd + 128);
-    float *wsum = reinterpret_cast<float *>(w2 + 128);
+    float *grow_all = reinterpret_cast<float *>(smem + SM::kF);         // [2][128]
+    float *ngd_all = grow_all + 256;                                     // [2][128]
+    uint32_t *w2_all = reinterpret_cast<uint32_t *>(ngd_all + 256);      // [2][128]
+    float *vcol_all = reinterpret_cast<float *>(w2_all + 256);           // [2][128]
+    float *wsum_all = vcol_all + 256;                                    // [2][4]
+    float *gpiv_all = wsum_all + 8;                                      // [2][4]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM::kBar);
-    uint64_t *bar_C = bars, *bar_B = bars + 1, *bar_X = bars + 2, *bar_cbi = bars + 3,
-             *bar_L = bars + 4, *bar_is = bars + 5, *bar_dr = bars + 6;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 7);
+    uint64_t *full_C = bars, *full_B = bars + 2, *full_X = bars + 4, *cb_done = bars + 6,
+             *inter_done = bars + 8, *L_ready = bars + 10, *is_done = bars + 12,
+             *drain_done = bars + 14, *hb_ready = bars + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
     int *s_err = reinterpret_cast<int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -160,18 +228,23 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const int nblk = int((t_end - t_begin + 127) / 128);
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(bar_C, 1);
-        ptx::mbar_init(bar_B, 1);
-        ptx::mbar_init(bar_X, 1);
-        ptx::mbar_init(bar_cbi, 1);
-        ptx::mbar_init(bar_L, 128);
-        ptx::mbar_init(bar_is, 1);
-        ptx::mbar_init(bar_dr, 128);
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(&full_C[s], 1);
+            ptx::mbar_init(&full_B[s], 1);
+            ptx::mbar_init(&full_X[s], 1);
+            ptx::mbar_init(&cb_done[s], 1);
+            ptx::mbar_init(&inter_done[s], 1);
+            ptx::mbar_init(&L_ready[s], kWgA);
+            ptx::mbar_init(&is_done[s], 1);
+            ptx::mbar_init(&drain_done[s], 128);
+        }
+        ptx::mbar_init(hb_ready, 128);
         *s_err = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tm_x);
         ptx::prefetch_tmap(&tm_b);
         ptx::prefetch_tmap(&tm_c);
+        ptx::prefetch_tmap(&tm_y);
     }
     if (warp == 1) {
         ptx::tmem_alloc(tmem_slot, kCols);
@@ -181,173 +254,295 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tL = tmem, tS = tmem + 64, tInter = tmem + 128, tIntra = tmem + 192;
     bool ok = true;
 
     if (warp == 0) {
+        // ---------------- TMA producer ----------------
         if (lane == 0) {
             for (int k = 0; k < nblk && ok; ++k) {
+                const int s = k & 1, u = k >> 1;
+                const uint32_t pp = (u - 1) & 1;  // phase of block k - 2 on this stage
                 const int t0 = int(t_begin + int64_t(k) * 128);
-                if (k > 0 && !ptx::mbar_wait(bar_cbi, (k - 1) & 1)) { ok = false; break; }
-                ptx::mbar_arrive_expect_tx(bar_C, 32768);
-                ptx::tma_load_4d(smem + SM::kC, &tm_c, bar_C, 0, g, t0, b);
-                ptx::tma_load_4d(smem + SM::kC + 16384, &tm_c, bar_C, 64, g, t0, b);
-                if (k > 0 && !ptx::mbar_wait(bar_is, (k - 1) & 1)) { ok = false; break; }
-                ptx::mbar_arrive_expect_tx(bar_B, 32768);
-                ptx::tma_load_4d(smem + SM::kB, &tm_b, bar_B, 0, g, t0, b);
-                ptx::tma_load_4d(smem + SM::kB + 16384, &tm_b, bar_B, 64, g, t0, b);
-                if (k > 0 && !ptx::mbar_wait(bar_dr, k & 1)) { ok = false; break; }
-                ptx::mbar_arrive_expect_tx(bar_X, 16384);
-                ptx::tma_load_4d(smem + SM::kX, &tm_x, bar_X, 0, h, t0, b);
+                if (u > 0 && !ptx::mbar_wait(&inter_done[s], pp)) { ok = false; break; }
+                ptx::mbar_arrive_expect_tx(&full_C[s], 32768);
+                ptx::tma_load_4d(smem + SM::kC + s * 32768, &tm_c, &full_C[s], 0, g, t0, b);
+                ptx::tma_load_4d(smem + SM::kC + s * 32768 + 16384, &tm_c, &full_C[s], 64, g, t0, b);
+                if (u > 0 && !ptx::mbar_wait(&is_done[s], pp)) { ok = false; break; }
+                ptx::mbar_arrive_expect_tx(&full_B[s], 32768);
+                ptx::tma_load_4d(smem + SM::kB + s * 32768, &tm_b, &full_B[s], 0, g, t0, b);
+                ptx::tma_load_4d(smem + SM::kB + s * 32768 + 16384, &tm_b, &full_B[s], 64, g, t0, b);
+                if (u > 0 && !ptx::mbar_wait(&drain_done[s], pp)) { ok = false; break; }
+                ptx::mbar_arrive_expect_tx(&full_X[s], 16384);
+                ptx::tma_load_4d(smem + SM::kX + s * 16384, &tm_x, &full_X[s], 0, h, t0, b);
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t sC = ptx::smem_u32(smem + SM::kC);
-            const uint32_t sB = ptx::smem_u32(smem + SM::kB);
-            const uint32_t sX = ptx::smem_u32(smem + SM::kX);
-            const uint32_t sXH = ptx::smem_u32(smem + SM::kXH);
-            for (int k = 0; k < nblk && ok; ++k) {
-                const uint32_t par = k & 1;
-                if (!ptx::mbar_wait(bar_C, par) || !ptx::mbar_wait(bar_B, par) ||
-                    !ptx::mbar_wait(bar_dr, par)) { ok = false; break; }
-                ptx::tc_fence_after();
-                // C B^T: K = state, both operands K-major
+        // ---------------- MMA issuer (event loop) ----------------
+        if (lane == 0 && nblk > 0) {
+            // Descriptor bases, computed once: an operand at byte offset o from its
+            // base is the base descriptor plus o >> 4 (start-address field; shared
+            // addresses stay below 2^18, so no carry leaves the field).
+            const uint64_t dCk = ptx::sdesc(ptx::smem_u32(smem + SM::kC), 16, 1024);
+            const uint64_t dBk = ptx::sdesc(ptx::smem_u32(smem + SM::kB), 16, 1024);
+            const uint64_t dBmn = ptx::sdesc(ptx::smem_u32(smem + SM::kB), 16384, 1024);
+            const uint64_t dX = ptx::sdesc(ptx::smem_u32(smem + SM::kX), 16384, 1024);
+            const uint64_t dXP = ptx::sdesc(ptx::smem_u32(smem + SM::kXP), 16384, 1024);
+            const uint64_t dHB = ptx::sdesc(ptx::smem_u32(smem + SM::kHB), 16384, 1024);
+            // K-major C / B over the state: K step 16 = 32 bytes, second 64-block 16 KB on
+            constexpr uint32_t kKoff[8] = {0, 2, 4, 6, 1024, 1026, 1028, 1030};
+            int k_inter = 0, k_is = 0, k_cb = 0;   // next block of each product
+            uint64_t idle_since = 0;
+            while (k_inter < nblk || k_is < nblk) {
+                bool progress = false;
+                // C h^T(k): the state entering block k is in its operand tile
+                if (k_inter < k_cb && ptx::mbar_test_wait(hb_ready, k_inter & 1)) {
+                    const int s = k_inter & 1;
+                    ptx::tc_fence_after();
+                    const uint64_t c0 = dCk + uint64_t(s * 2048);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    ptx::mma_bf16_ss(tmem,
-                                     ptx::sdesc(sC + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                                     ptx::sdesc(sB + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                                     kIdCB, ks != 0);
-                // C h^T: K = state; h stored [n][p] (MN-major, 16 state rows per step)
+                    for (int ks = 0; ks < 8; ++ks)   // MN-major operand: K step 16 rows = 2 KB
+                        ptx::mma_bf16_ss(tmem + 256 + 64 * s, c0 + kKoff[ks],
+                                         dHB + uint64_t(ks * 128), kIdKmn, ks != 0);
+                    ptx::mma_commit(&inter_done[s]);
+                    ++k_inter;
+                    progress = true;
+                }
+                // L x(k) and S^T(k): block k's decay operand and w o x are ready and
+                // its intra accumulator has been drained (block k - 2)
+                if (k_is < k_cb) {
+                    const int s = k_is & 1;
+                    const uint32_t par = (k_is >> 1) & 1;
+                    if (ptx::mbar_test_wait(&L_ready[s], par) &&
+                        (k_is < 2 || ptx::mbar_test_wait(&drain_done[s], par ^ 1))) {
+                        ptx::tc_fence_after();
+                        const uint64_t x0 = dX + uint64_t(s * 1024);
+                        const uint64_t xp0 = dXP + uint64_t(s * 1024);
+                        const uint64_t bmn0 = dBmn + uint64_t(s * 2048);
+                        const uint32_t t_cbl = tmem + 128 * s;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    ptx::mma_bf16_ss(tInter,
-                                     ptx::sdesc(sC + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                                     ptx::sdesc(sXH + ks * 2048, 16384, 1024), kIdKmn, ks != 0);
-                ptx::mma_commit(bar_cbi);
-                if (!ptx::mbar_wait(bar_L, par)) { ok = false; break; }
-                ptx::tc_fence_after();
-                // L x: A = L from tensor memory (8 columns per 16 tokens), x [j][p] MN-major
+                        for (int ks = 0; ks < 8; ++ks)
+                            ptx::mma_bf16_ts(tmem + 384 + 64 * s, t_cbl + ks * 8,
+                                             x0 + uint64_t(ks * 128), kIdKmn, ks != 0);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    ptx::mma_bf16_ts(tIntra, tL + ks * 8, ptx::sdesc(sX + ks * 2048, 16384, 1024),
-                                     kIdKmn, ks != 0);
-                // S^T = B^T (w o x): A = B^T (MN-major, the two state halves 16 KB apart)
+                        for (int ks = 0; ks < 8; ++ks)
+                            ptx::mma_bf16_ss(t_cbl + 64, bmn0 + uint64_t(ks * 128),
+                                             xp0 + uint64_t(ks * 128), kIdState, ks != 0);
+                        ptx::mma_commit(&is_done[s]);
+                        ++k_is;
+                        progress = true;
+                    }
+                }
+                // C B^T(k): its operands landed and its stage's tensor memory is free:
+                // L x and S^T of block k - 2 done, and S^T(k - 2) absorbed into the
+                // state -- known once C h^T(k - 1) was issued, which waited for it
+                if (k_cb < nblk && k_cb <= k_is + 1) {
+                    const int s = k_cb & 1;
+                    const uint32_t par = (k_cb >> 1) & 1;
+                    if (ptx::mbar_test_wait(&full_C[s], par) && ptx::mbar_test_wait(&full_B[s], par) &&
+                        (k_cb < 2 || (k_inter >= k_cb &&
+                                      ptx::mbar_test_wait(&is_done[s], par ^ 1)))) {
+                        ptx::tc_fence_after();
+                        const uint64_t c0 = dCk + uint64_t(s * 2048), b0 = dBk + uint64_t(s * 2048);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    ptx::mma_bf16_ss(tS, ptx::sdesc(sB + ks * 2048, 16384, 1024),
-                                     ptx::sdesc(sXH + ks * 2048, 16384, 1024), kIdState, ks != 0);
-                ptx::mma_commit(bar_is);
+                        for (int ks = 0; ks < 8; ++ks)
+                            ptx::mma_bf16_ss(tmem + 128 * s, c0 + kKoff[ks], b0 + kKoff[ks], kIdCB,
+                                             ks != 0);
+                        ptx::mma_commit(&cb_done[s]);
+                        ++k_cb;
+                        progress = true;
+                    }
+                }
+                if (progress) {
+                    idle_since = 0;
+                } else {
+                    const uint64_t now = ptx::globaltimer_ns();
+                    if (!idle_since) idle_since = now;
+                    else if (now - idle_since > 2000000000ull) { ok = false; break; }
+                }
             }
-            // the last commit must land before tensor memory is released
-            if (ok && nblk > 0 && !ptx::mbar_wait(bar_is, (nblk - 1) & 1)) ok = false;
+            // every commit must land before tensor memory is released
+            if (ok && !ptx::mbar_wait(&is_done[(nblk - 1) & 1], ((nblk - 1) >> 1) & 1)) ok = false;
+            if (ok && !ptx::mbar_wait(&inter_done[(nblk - 1) & 1], ((nblk - 1) >> 1) & 1)) ok = false;
+        }
+    } else if (warp < 10) {
+        // ---------------- warpgroup A: w o x and the decay operand ----------------
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;          // which column blocks of the quarter
+        const int r = 32 * q + lane;
+        const int ta = threadIdx.x - 64;           // 0..255
+        const uint32_t lane_off = uint32_t(32 * q) << 16;
+        const float Ah = p.A[h];
+        const float *dtp = p.dt + int64_t(b) * p.dt_sb + h;
+        float dt_next = 0.f;
+        if (half == 0) dt_next = (t_begin + r < t_end) ? __ldg(dtp + (t_begin + r) * p.dt_sl) : 0.f;
+        for (int k = 0; k < nblk; ++k) {
+            const int s = k & 1;
+            const uint32_t par = (k >> 1) & 1;
+            float *grow = grow_all + 128 * s;
+            float *ngd = ngd_all + 128 * s;
+            uint32_t *w2 = w2_all + 128 * s;
+            float *vcol = vcol_all + 128 * s;
+            float *gpiv = gpiv_all + 4 * s;
+            if (half == 0) {
+                const int64_t t = t_begin + int64_t(k) * 128 + r;
+                const float dtr = dt_next;
+                if (k + 1 < nblk) dt_next = (t + 128 < t_end) ? __ldg(dtp + (t + 128) * p.dt_sl) : 0.f;
+                float gr, gend;
+                block_cumsum(Ah * dtr, q, lane, 1, wsum_all, gr, gend);
+                const float ngr = log2f(dtr) - gr;     // -inf for dt = 0
+                grow[r] = gr;
+                ngd[r] = ngr;
+                const float w = ex2(gend - gr) * dtr;
+                w2[r] = pack_bf16(w, w);
+                // warp q holds column block q; its pivot is the block's last row
+                const float gp = __shfl_sync(0xffffffffu, gr, 31);
+                vcol[r] = ex2(gp + ngr);               // 2^(g_p - g_r) dt_r
+                if (lane == 31) gpiv[q] = gp;
+            }
+            asm volatile("bar.sync 3, 256;" ::: "memory");
+            const float gr = grow[r];
+
+            // w o x into this stage's buffer (free once S(k - 2) has completed);
+            // it does not need C B^T, so it runs while that product is computed
+            if (!__all_sync(0xffffffffu,
+                            ptx::mbar_wait(&full_X[s], par) &&
+                                (k < 2 || ptx::mbar_wait(&is_done[s], par ^ 1)))) {
+                ok = false;
+                break;
+            }
+            {
+                const uint4 *xs = reinterpret_cast<const uint4 *>(smem + SM::kX + s * 16384);
+                uint4 *xp = reinterpret_cast<uint4 *>(smem + SM::kXP + s * 16384);
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr) {
+                    const int chunk = ta + kWgA * rr;    // 16-byte chunk; row j = chunk / 8
+                    const uint32_t wv = w2[chunk >> 3];
+                    const __nv_bfloat162 wb = *reinterpret_cast<const __nv_bfloat162 *>(&wv);
+                    uint4 v = xs[chunk];
+                    __nv_bfloat162 *v2 = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) v2[kk] = __hmul2(v2[kk], wb);
+                    xp[chunk] = v;
+                }
+            }
+            ptx::fence_proxy_async_smem();
+
+            // L, in place over C B^T: this warp owns column blocks half and
+            // half + 2 of its rows (blocks past the diagonal block q are zero).
+            // Every read of the stage's C B^T completes before any write.
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&cb_done[s], par))) { ok = false; break; }
+            ptx::tc_fence_after();
+            {
+                const uint32_t tL = tmem + 128 * s + lane_off;
+                const int c0 = half, c1 = half + 2;
+                uint32_t v0[32], v1[32], out[16];
+                if (c0 <= q) ptx::tmem_ld32(tL + 32 * c0, v0);
+                if (c1 <= q) ptx::tmem_ld32(tL + 32 * c1, v1);
+                ptx::tmem_ld_wait();
+                ptx::tc_fence_before();
+                asm volatile("bar.sync 3, 256;" ::: "memory");
+                ptx::tc_fence_after();
+                if (c0 <= q) {
+                    if (c0 == q) l_block(v0, 32 * c0, true, r, gr, ngd, out);
+                    else l_block_below(v0, 32 * c0, ex2(gr - gpiv[c0]), vcol, out);
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) out[jj] = 0u;
+                }
+                ptx::tmem_st16(tL + 16 * c0, out);
+                if (c1 <= q) {
+                    if (c1 == q) l_block(v1, 32 * c1, true, r, gr, ngd, out);
+                    else l_block_below(v1, 32 * c1, ex2(gr - gpiv[c1]), vcol, out);
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) out[jj] = 0u;
+                }
+                ptx::tmem_st16(tL + 16 * c1, out);
+                ptx::tmem_st_wait();
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&L_ready[s]);
         }
     } else {
+        // ---------------- warpgroup B: carried state and y ----------------
         const int q = warp & 3;
-        const int r = 32 * q + lane;               // tile row i, state row n, TMEM lane
+        const int r = 32 * q + lane;
         const uint32_t lane_off = uint32_t(32 * q) << 16;
         const float Ah = p.A[h];
         const float Dh = p.D ? p.D[h] : 0.f;
         const float2 D2 = make_float2(Dh, Dh);
-        uint8_t *xh = smem + SM::kXH;
-        const uint8_t *xs = smem + SM::kX;
+        uint8_t *hb = smem + SM::kHB;
         const size_t slab = size_t(b) * p.H + h;
-        // carried state row n = r, pairs of headdim values (2m, 2m + 1), fp32
-        float2 hreg[32];
+        float2 hreg[32];   // state row n = r, headdim pairs (2m, 2m + 1), fp32
         const float *hin = p.h_in ? p.h_in + (size_t(seg) * p.B * p.H + slab) * 8192 : nullptr;
 #pragma unroll
         for (int m = 0; m < 32; ++m)
             hreg[m] = hin ? make_float2(hin[(2 * m) * 128 + r], hin[(2 * m + 1) * 128 + r])
                           : make_float2(0.f, 0.f);
-        write_state_row(xh, r, hreg);
+        write_state_row(hb, r, hreg);
         ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(bar_dr);
+        ptx::mbar_arrive(hb_ready);
 
         const float *dtp = p.dt + int64_t(b) * p.dt_sb + h;
         float dt_next = (t_begin + r < t_end) ? __ldg(dtp + (t_begin + r) * p.dt_sl) : 0.f;
         for (int k = 0; k < nblk; ++k) {
-            const uint32_t par = k & 1;
+            const int s = k & 1;
+            const uint32_t par = (k >> 1) & 1;
             const int64_t t = t_begin + int64_t(k) * 128 + r;
-            const bool real = t < t_end;
             const float dtr = dt_next;
-            if (k + 1 < nblk) {            // the next block's dt, one block ahead
-                const int64_t tn = t + 128;
-                dt_next = tn < t_end ? __ldg(dtp + tn * p.dt_sl) : 0.f;
-            }
-            // ---- block-local cumulative sum of A dt (log2 units) ----
-            float s = Ah * dtr;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float o = __shfl_up_sync(0xffffffffu, s, off);
-                if (lane >= off) s += o;
-            }
-            if (lane == 31) wsum[q] = s;
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            float pre = 0.f;
-            for (int qq = 0; qq < q; ++qq) pre += wsum[qq];
-            const float tot = ((wsum[0] + wsum[1]) + wsum[2]) + wsum[3];
-            const float gr = (pre + s) * kLog2e;
-            const float gend = tot * kLog2e;
-            ngd[r] = log2f(dtr) - gr;                  // -inf for dt = 0
-            const float w = ex2(gend - gr) * dtr;
-            w2[r] = pack_bf16(w, w);
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (k + 1 < nblk) dt_next = (t + 128 < t_end) ? __ldg(dtp + (t + 128) * p.dt_sl) : 0.f;
+            float gr, gend;
+            block_cumsum(Ah * dtr, q, lane, 2, wsum_all + 4, gr, gend);
+            asm volatile("bar.sync 2, 128;" ::: "memory");   // wsum reads done before reuse
 
-            // ---- L: causal-selected decay of C B^T, in place, bf16 pairs ----
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar_cbi, par))) { ok = false; break; }
+            // state: h(k + 1) = 2^(g_end) h(k) + S(k); its bf16 copy feeds C h^T(k + 1)
+            // once C h^T(k) has read the current one
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&is_done[s], par) &&
+                                             ptx::mbar_wait(&inter_done[s], par))) {
+                ok = false;
+                break;
+            }
             ptx::tc_fence_after();
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {   // column blocks of 32
-                uint32_t out[16];
-                if (cb <= q) {                 // rows of warp q see columns j <= 32 q + 31
-                    uint32_t v[32];
-                    ptx::tmem_ld32(tmem + lane_off + 32 * cb, v);
+            {
+                const float dend = ex2(gend);
+                const float2 d2 = make_float2(dend, dend);
+#pragma unroll
+                for (int cb = 0; cb < 2; ++cb) {
+                    uint32_t sv[32];
+                    ptx::tmem_ld32(tmem + 128 * s + 64 + lane_off + 32 * cb, sv);
                     ptx::tmem_ld_wait();
-                    l_block(v, 32 * cb, cb == q, r, gr, ngd, out);
-                } else {
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) out[jj] = 0u;
+                    for (int m = 0; m < 16; ++m)
+                        hreg[16 * cb + m] =
+                            __ffma2_rn(d2, hreg[16 * cb + m],
+                                       make_float2(__uint_as_float(sv[2 * m]),
+                                                   __uint_as_float(sv[2 * m + 1])));
                 }
-                ptx::tmem_st16(tL + lane_off + 16 * cb, out);
-            }
-            ptx::tmem_st_wait();
-
-            // ---- w o x for the state product (inter has consumed the state operand) ----
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar_X, par))) { ok = false; break; }
-#pragma unroll
-            for (int rr = 0; rr < 8; ++rr) {
-                const int chunk = r + 128 * rr;      // 16-byte chunk; row j = chunk / 8
-                const uint32_t wv = w2[chunk >> 3];
-                const __nv_bfloat162 wb = *reinterpret_cast<const __nv_bfloat162 *>(&wv);
-                uint4 v = reinterpret_cast<const uint4 *>(xs)[chunk];
-                __nv_bfloat162 *v2 = reinterpret_cast<__nv_bfloat162 *>(&v);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) v2[kk] = __hmul2(v2[kk], wb);
-                reinterpret_cast<uint4 *>(xh)[chunk] = v;
+                write_state_row(hb, r, hreg);
             }
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_L);
+            ptx::mbar_arrive(hb_ready);
 
-            // ---- drain: y rows, then the carried state ----
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar_is, par))) { ok = false; break; }
-            ptx::tc_fence_after();
+            // y(k) = 2^(g_i) inter + intra + D x, written over this block's x tile
+            // (each thread reads its x row before writing its y row there), then
+            // stored as one tile by TMA (rows past the sequence end are clipped)
             {
                 const float e_i = ex2(gr);
                 const float2 e2 = make_float2(e_i, e_i);
-                const uint8_t *xrow = xs + r * 128;
-                __nv_bfloat16 *yrow = p.y + int64_t(b) * p.y_sb + t * p.y_sl + int64_t(h) * p.y_sh;
+                uint8_t *tile = smem + SM::kX + s * 16384;
+                uint8_t *row = tile + r * 128;
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t a[16], d[16];
-                    ptx::tmem_ld16(tInter + lane_off + 16 * cb, a);
-                    ptx::tmem_ld16(tIntra + lane_off + 16 * cb, d);
+                    ptx::tmem_ld16(tmem + 256 + 64 * s + lane_off + 16 * cb, a);
+                    ptx::tmem_ld16(tmem + 384 + 64 * s + lane_off + 16 * cb, d);
                     ptx::tmem_ld_wait();
 #pragma unroll
                     for (int c4 = 0; c4 < 2; ++c4) {
                         const int ch = 2 * cb + c4;
-                        const uint4 xv = *reinterpret_cast<const uint4 *>(xrow + ((ch ^ (r & 7)) << 4));
+                        uint4 *cp = reinterpret_cast<uint4 *>(row + ((ch ^ (r & 7)) << 4));
+                        const uint4 xv = *cp;
                         const uint32_t *xu = reinterpret_cast<const uint32_t *>(&xv);
                         uint32_t o[4];
 #pragma unroll
@@ -359,32 +554,21 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                             acc = __ffma2_rn(unpack_bf16(xu[kk]), D2, acc);
                             o[kk] = pack_bf16(acc.x, acc.y);
                         }
-                        if (real)
-                            *reinterpret_cast<uint4 *>(yrow + 8 * ch) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *cp = make_uint4(o[0], o[1], o[2], o[3]);
                     }
                 }
-            }
-            {
-                const float dend = ex2(gend);
-                const float2 d2 = make_float2(dend, dend);
-#pragma unroll
-                for (int cb = 0; cb < 2; ++cb) {
-                    uint32_t sv[32];
-                    ptx::tmem_ld32(tS + lane_off + 32 * cb, sv);
-                    ptx::tmem_ld_wait();
-#pragma unroll
-                    for (int m = 0; m < 16; ++m)
-                        hreg[16 * cb + m] =
-                            __ffma2_rn(d2, hreg[16 * cb + m],
-                                       make_float2(__uint_as_float(sv[2 * m]),
-                                                   __uint_as_float(sv[2 * m + 1])));
+                ptx::fence_proxy_async_smem();
+                asm volatile("bar.sync 2, 128;" ::: "memory");
+                if (warp == 10 && lane == 0) {
+                    ptx::tma_store_4d(&tm_y, tile, 0, h, int(t_begin + int64_t(k) * 128), b);
+                    ptx::bulk_commit_group();
+                    ptx::bulk_wait_group_read0();   // the tile is reloaded after drain_done
                 }
-                write_state_row(xh, r, hreg);
             }
-            ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_dr);
+            ptx::mbar_arrive(&drain_done[s]);
         }
+        if (warp == 10 && lane == 0) ptx::bulk_wait_group0();
         if (ok && p.h_out) {
             float *ho = p.h_out + slab * 8192;
 #pragma unroll
@@ -424,6 +608,9 @@ cudaError_t launch_fused(const Args &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if ((e = make_tmap_bf16(&tm_b, a.Bm, 4, bd, bs, box)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16(&tm_c, a.Cm, 4, bd, cs, box)) != cudaSuccess) return e;
+    CUtensorMap tm_y;
+    const uint64_t ys[3] = {uint64_t(a.y_sh) * 2, uint64_t(a.y_sl) * 2, uint64_t(a.y_sb) * 2};
+    if ((e = make_tmap_bf16(&tm_y, a.y, 4, xd, ys, box)) != cudaSuccess) return e;
     unsigned int *err = nullptr;
     if ((e = device_error_word(&err)) != cudaSuccess) return e;
     FusedParams p{};
@@ -449,7 +636,7 @@ cudaError_t launch_fused(const Args &a, cudaStream_t s) {
     e = cudaFuncSetAttribute(k_ssd_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const unsigned units = unsigned(d.B * d.H) * unsigned(p.nseg);
-    k_ssd_fused<<<units, 192, smem, s>>>(tm_x, tm_b, tm_c, p);
+    k_ssd_fused<<<units, kThreads, smem, s>>>(tm_x, tm_b, tm_c, tm_y, p);
     return cudaGetLastError();
 }
 
