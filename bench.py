@@ -229,7 +229,7 @@ def run_reference(args, w, world, rank):
     orc.recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
                    inp["initial_states"], ngroups=w.ngroups, slabs=slabs_all[:cores])
     per_slab = max((time.perf_counter() - t0) / cores, 1e-4)  # wall per slab at full width
-    budget = 150.0 / max(args.steps + args.warmup, 1)
+    budget = args.ref_seconds / max(args.steps + args.warmup, 1)
     n = int(max(1, min(len(slabs_all), budget / per_slab)))
     sample = slabs_all[:n]
     step = lambda: orc.recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
@@ -287,6 +287,8 @@ def main():
     ap.add_argument("--workload", default=gen.HEADLINE, choices=sorted(gen.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=150.0,
+                    help="wall-time budget of the whole --impl reference run")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = gen.WORKLOADS[args.workload]
