@@ -35,7 +35,7 @@
 // warpgroup A (the decay operand L), warps 8..11 = warpgroup S (w o x and the
 // state), warps 12..15 = warpgroup Y (y and its TMA store).  A math thread
 // owns tile row / state row r = its TMEM lane.  One CTA per SM (all 512 TMEM
-// columns, 212 KB of shared memory).
+// columns, 211 KB of shared memory).
 #include "ptx_sm100.cuh"
 #include "ssd_internal.h"
 #include "ssd_tc.cuh"
@@ -70,13 +70,14 @@ struct FusedParams {
 struct FusedSmem {
     static constexpr int kC = 0;          // 2 stages x 2 x [128 tokens][128 B]  C, K-major
     static constexpr int kB = 65536;      // 2 stages x 2 x [128 tokens][128 B]  B, K-major
-    static constexpr int kX = 131072;     // 2 stages x [128 tokens][128 B]      x, then y
+    static constexpr int kX = 131072;     // 2 stages x [128 tokens][128 B]      x, MN-major
     static constexpr int kXP = 163840;    // [128 tokens][128 B]                 w o x
-    static constexpr int kHB = 180224;    // 2 x [128 n][128 B]                  bf16 state
-    static constexpr int kF = 212992;     // per stage: g, ngd, vcol [128]; gpiv [4]; g_end
-    static constexpr int kNF = 2 * 392;   // two records (see kRec)
+    static constexpr int kHB = 180224;    // [128 n][128 B]                      bf16 state
+    static constexpr int kY = 196608;     // [128 tokens][128 B]                 y staging
+    static constexpr int kF = 212992;     // 4 records: g, ngd, vcol [128]; gpiv [4]; g_end
+    static constexpr int kNF = 4 * 392;   // four records (see kRec)
     static constexpr int kBar = kF + ((kNF * 4 + 7) & ~7);
-    static constexpr int kNBar = 25;
+    static constexpr int kNBar = 29;
     static constexpr int kBytes = kBar + kNBar * 8 + 8;
 };
 static_assert(FusedSmem::kBytes <= 232448, "shared memory above the per-CTA limit");
@@ -86,7 +87,10 @@ constexpr int kWgA = 192;                 // warpgroup A threads (warps 2..7)
 // floats of one block's cumulative-sum record (389 used), a multiple of 4 so
 // that both records' arrays stay 16-byte aligned for vector loads
 constexpr int kRec = 392;
-static_assert(kRec % 4 == 0 && FusedSmem::kNF == 2 * kRec && FusedSmem::kF % 16 == 0,
+constexpr int kNRec = 4;                  // records in the ring
+// warps that read a record: warpgroups A (6), S (4) and Y (4); each releases it once
+constexpr int kRecReaders = 14;
+static_assert(kRec % 4 == 0 && FusedSmem::kNF == kNRec * kRec && FusedSmem::kF % 16 == 0,
               "record layout");
 
 // device error flags
@@ -222,14 +226,15 @@ __device__ __forceinline__ void build_record(const float (&dt)[4], float Ah, int
 }
 
 // Named barriers (0 is __syncthreads): 4 + q = the two warps of warpgroup A
-// on TMEM lane quarter q (q = 2, 3), 9 = warpgroup Y.
+// on TMEM lane quarter q (q = 2, 3), 8 and 9 = warpgroup Y.
 //
 // Block k uses stage s = k & 1 of the double buffers.  Tensor memory:
 // [128 s, +128) = C B^T, then L in its first 64 columns and the intra
 // accumulator in its last 64; [256 + 64 s, +64) = S^T; [384 + 64 s, +64) =
-// inter.  The bf16 state entering block k is in operand buffer k & 1; w o x
-// has one buffer (w o x of block k + 1 is written after B^T (w o x)(k) has
-// completed, which the state update of block k waited for).
+// inter.  w o x, the bf16 state operand and the y staging tile have one
+// buffer each: w o x(k + 1) is written once B^T (w o x)(k) has completed, the
+// state entering block k + 1 once C h^T(k) has read the one entering block
+// k, and y(k) once the TMA store of y(k - 1) has read its tile.
 //
 // Every wait below names the phase of a barrier that cannot have advanced a
 // further phase yet: the later phase depends on work that the waiter itself
@@ -248,12 +253,12 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         if (threadIdx.x == 0) atomicOr(p.err, kErrSmemAlign);
         return;
     }
-    float *rec_all = reinterpret_cast<float *>(smem + SM::kF);   // [2][kRec]
+    float *rec_all = reinterpret_cast<float *>(smem + SM::kF);   // [kNRec][kRec]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM::kBar);
     uint64_t *full_C = bars, *full_B = bars + 2, *full_X = bars + 4, *cb_done = bars + 6,
              *s_done = bars + 8, *inter_done = bars + 10, *intra_done = bars + 12,
-             *sc_ready = bars + 14, *L_ready = bars + 16, *st_done = bars + 18,
-             *drain_done = bars + 20, *xfree = bars + 22, *xp_ready = bars + 24;
+             *L_ready = bars + 14, *st_done = bars + 16, *drain_done = bars + 18,
+             *xp_ready = bars + 20, *sc_ready = bars + 21, *rec_free = bars + 25;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + SM::kNBar);
     int *s_err = reinterpret_cast<int *>(tmem_slot + 1);
 
@@ -278,13 +283,15 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             ptx::mbar_init(&s_done[s], 1);
             ptx::mbar_init(&inter_done[s], 1);
             ptx::mbar_init(&intra_done[s], 1);
-            ptx::mbar_init(&sc_ready[s], 32);
             ptx::mbar_init(&L_ready[s], kWgA);
             ptx::mbar_init(&st_done[s], 128);
             ptx::mbar_init(&drain_done[s], 128);
-            ptx::mbar_init(&xfree[s], 1);
         }
         ptx::mbar_init(xp_ready, 128);
+        for (int i = 0; i < kNRec; ++i) {
+            ptx::mbar_init(&sc_ready[i], 32);
+            ptx::mbar_init(&rec_free[i], kRecReaders);
+        }
         *s_err = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tm_x);
@@ -318,48 +325,81 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         // ---------------- TMA producer and the cumulative-sum record ----------------
         const float Ah = p.A[h];
         const float *dtp = p.dt + int64_t(b) * p.dt_sb + h;
+        // Event loop, warp-uniform: lane 0 tests the barriers and issues the
+        // copies, the whole warp builds the records.  Each stream goes ahead as
+        // soon as its own buffer is free, so no copy waits behind another.
         float dtn[4];
         load_dt4(dtp, p.dt_sl, t_begin, t_end, lane, dtn);
-        for (int k = 0; k < nblk; ++k) {
-            const int s = k & 1, u = k >> 1;
-            const uint32_t pp = (u - 1) & 1;  // phase of block k - 2 on this stage
-            const int t0 = int(t_begin + int64_t(k) * 128);
-            bool good = true;
+        int kb = 0, kc = 0, kx = 0, kr = 0;   // next block of each stream
+        uint64_t idle_since = 0;
+        while (kb < nblk || kc < nblk || kx < nblk || kr < nblk) {
+            int fired = 0;   // bit i: stream i issued (lane 0's decision)
             if (lane == 0) {
                 // B: read by C B^T(k - 2) and B^T (w o x)(k - 2)
-                if (u > 0) good = ptx::mbar_wait(&cb_done[s], pp) && ptx::mbar_wait(&s_done[s], pp);
-                if (good) {
-                    ptx::mbar_arrive_expect_tx(&full_B[s], 32768);
-                    ptx::tma_load_4d(smem + SM::kB + s * 32768, &tm_b, &full_B[s], 0, g, t0, b);
-                    ptx::tma_load_4d(smem + SM::kB + s * 32768 + 16384, &tm_b, &full_B[s], 64, g,
-                                     t0, b);
+                if (kb < nblk) {
+                    const int s = kb & 1;
+                    const uint32_t pp = ((kb >> 1) - 1) & 1;
+                    if (kb < 2 || (ptx::mbar_test_wait(&cb_done[s], pp) &&
+                                   ptx::mbar_test_wait(&s_done[s], pp))) {
+                        const int t0 = int(t_begin + int64_t(kb) * 128);
+                        ptx::mbar_arrive_expect_tx(&full_B[s], 32768);
+                        ptx::tma_load_4d(smem + SM::kB + s * 32768, &tm_b, &full_B[s], 0, g, t0, b);
+                        ptx::tma_load_4d(smem + SM::kB + s * 32768 + 16384, &tm_b, &full_B[s], 64,
+                                         g, t0, b);
+                        fired |= 1;
+                    }
                 }
                 // C: read by C B^T(k - 2) and C h^T(k - 2), issued after it
-                if (good && u > 0) good = ptx::mbar_wait(&inter_done[s], pp);
-                if (good) {
-                    ptx::mbar_arrive_expect_tx(&full_C[s], 32768);
-                    ptx::tma_load_4d(smem + SM::kC + s * 32768, &tm_c, &full_C[s], 0, g, t0, b);
-                    ptx::tma_load_4d(smem + SM::kC + s * 32768 + 16384, &tm_c, &full_C[s], 64, g,
-                                     t0, b);
+                if (kc < nblk) {
+                    const int s = kc & 1;
+                    const uint32_t pp = ((kc >> 1) - 1) & 1;
+                    if (kc < 2 || ptx::mbar_test_wait(&inter_done[s], pp)) {
+                        const int t0 = int(t_begin + int64_t(kc) * 128);
+                        ptx::mbar_arrive_expect_tx(&full_C[s], 32768);
+                        ptx::tma_load_4d(smem + SM::kC + s * 32768, &tm_c, &full_C[s], 0, g, t0, b);
+                        ptx::tma_load_4d(smem + SM::kC + s * 32768 + 16384, &tm_c, &full_C[s], 64,
+                                         g, t0, b);
+                        fired |= 2;
+                    }
                 }
-                // x and the record: the x tile holds y(k - 2) until its TMA store has
-                // read it, and the record of block k - 2 is in use until the state
-                // update of block k - 2 (every other reader of it is done before that
-                // store)
-                if (good && u > 0)
-                    good = ptx::mbar_wait(&xfree[s], pp) && ptx::mbar_wait(&st_done[s], pp);
-                if (good) {
-                    ptx::mbar_arrive_expect_tx(&full_X[s], 16384);
-                    ptx::tma_load_4d(smem + SM::kX + s * 16384, &tm_x, &full_X[s], 0, h, t0, b);
+                // x: read by w o x(k - 2) and L x(k - 2), issued after it
+                if (kx < nblk) {
+                    const int s = kx & 1;
+                    const uint32_t pp = ((kx >> 1) - 1) & 1;
+                    if (kx < 2 || ptx::mbar_test_wait(&intra_done[s], pp)) {
+                        const int t0 = int(t_begin + int64_t(kx) * 128);
+                        ptx::mbar_arrive_expect_tx(&full_X[s], 16384);
+                        ptx::tma_load_4d(smem + SM::kX + s * 16384, &tm_x, &full_X[s], 0, h, t0, b);
+                        fired |= 4;
+                    }
+                }
+                // the record of block k - 4 is in use until every reader released it
+                if (kr < nblk &&
+                    (kr < kNRec || ptx::mbar_test_wait(&rec_free[kr & 3], ((kr >> 2) - 1) & 1)))
+                    fired |= 8;
+                if (fired) {
+                    idle_since = 0;
+                } else {
+                    const uint64_t now = ptx::globaltimer_ns();
+                    if (!idle_since) idle_since = now;
+                    else if (now - idle_since > 2000000000ull) fired = -1;
                 }
             }
-            if (!__shfl_sync(0xffffffffu, good ? 1 : 0, 0)) { ok = false; break; }
-            float dtv[4];
+            fired = __shfl_sync(0xffffffffu, fired, 0);
+            if (fired < 0) { ok = false; break; }
+            kb += fired & 1;
+            kc += (fired >> 1) & 1;
+            kx += (fired >> 2) & 1;
+            if (fired & 8) {
+                float dtv[4];
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) dtv[qq] = dtn[qq];
-            if (k + 1 < nblk) load_dt4(dtp, p.dt_sl, t_begin + int64_t(k + 1) * 128, t_end, lane, dtn);
-            build_record(dtv, Ah, lane, rec_all + kRec * s);
-            ptx::mbar_arrive(&sc_ready[s]);
+                for (int qq = 0; qq < 4; ++qq) dtv[qq] = dtn[qq];
+                if (kr + 1 < nblk)
+                    load_dt4(dtp, p.dt_sl, t_begin + int64_t(kr + 1) * 128, t_end, lane, dtn);
+                build_record(dtv, Ah, lane, rec_all + kRec * (kr & 3));
+                ptx::mbar_arrive(&sc_ready[kr & 3]);
+                ++kr;
+            }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer (event loop) ----------------
@@ -406,11 +446,10 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                         (k_in < 2 || ptx::mbar_test_wait(&drain_done[s], par ^ 1))) {
                         ptx::tc_fence_after();
                         const uint64_t c0 = dCk + uint64_t(s * 2048);
-                        const uint64_t h0 = dHB + uint64_t(s * 1024);
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks)
                             ptx::mma_bf16_ss(tmem + 384 + 64 * s, c0 + kKoff[ks],
-                                             h0 + uint64_t(ks * 128), kIdKmn, ks != 0);
+                                             dHB + uint64_t(ks * 128), kIdKmn, ks != 0);
                         ptx::mma_commit(&inter_done[s]);
                         ++k_in;
                         progress = true;
@@ -486,13 +525,13 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         for (int k = 0; k < nblk; ++k) {
             const int s = k & 1;
             const uint32_t par = (k >> 1) & 1;
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&sc_ready[s], par) &&
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&sc_ready[k & 3], (k >> 2) & 1) &&
                                              ptx::mbar_wait(&cb_done[s], par))) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-            const float *rec = rec_all + kRec * s;
+            const float *rec = rec_all + kRec * (k & 3);
             const float gr = rec[r];
             const uint32_t tL = tmem + 128 * s + lane_off;
             uint32_t v[32], out[16];
@@ -522,6 +561,8 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
             ptx::mbar_arrive(&L_ready[s]);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&rec_free[k & 3]);
         }
     } else if (warp < 12) {
         // ---------------- warpgroup S: w o x and the carried state ----------------
@@ -530,39 +571,55 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         const uint32_t lane_off = uint32_t(32 * q) << 16;
         uint8_t *hb = smem + SM::kHB;
         uint8_t *xprow = smem + SM::kXP + r * 128;
-        for (int k = 0; k < nblk; ++k) {
+        // w o x(k), row r, into the single w o x buffer
+        // g_end of the record consumed last, kept for that block's state update
+        float gend_k = 0.f;
+        auto build_wx = [&](int k) -> bool {
             const int s = k & 1;
             const uint32_t par = (k >> 1) & 1;
-            // w o x(k), row r: its buffer is free since B^T (w o x)(k - 1) completed
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&sc_ready[s], par) &&
-                                             ptx::mbar_wait(&full_X[s], par))) {
-                ok = false;
-                break;
-            }
-            const float *rec = rec_all + kRec * s;
-            const float gend = rec[388];
-            {
-                const float w = ex2(gend + rec[128 + r]);   // 2^(g_end - g_r) dt_r
-                const __nv_bfloat162 wb = __floats2bfloat162_rn(w, w);
-                const uint8_t *xrow = smem + SM::kX + s * 16384 + r * 128;
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&sc_ready[k & 3], (k >> 2) & 1) &&
+                                             ptx::mbar_wait(&full_X[s], par)))
+                return false;
+            const float *rec = rec_all + kRec * (k & 3);
+            gend_k = rec[388];
+            const float w = ex2(gend_k + rec[128 + r]);   // 2^(g_end - g_r) dt_r
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&rec_free[k & 3]);
+            const __nv_bfloat162 wb = __floats2bfloat162_rn(w, w);
+            const uint8_t *xrow = smem + SM::kX + s * 16384 + r * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int off = (c ^ (r & 7)) << 4;   // swizzled: conflict-free per 8 rows
-                    uint4 v = *reinterpret_cast<const uint4 *>(xrow + off);
-                    __nv_bfloat162 *v2 = reinterpret_cast<__nv_bfloat162 *>(&v);
+            for (int c = 0; c < 8; ++c) {
+                const int off = (c ^ (r & 7)) << 4;   // swizzled: conflict-free per 8 rows
+                uint4 v = *reinterpret_cast<const uint4 *>(xrow + off);
+                __nv_bfloat162 *v2 = reinterpret_cast<__nv_bfloat162 *>(&v);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) v2[kk] = __hmul2(v2[kk], wb);
-                    *reinterpret_cast<uint4 *>(xprow + off) = v;
-                }
+                for (int kk = 0; kk < 4; ++kk) v2[kk] = __hmul2(v2[kk], wb);
+                *reinterpret_cast<uint4 *>(xprow + off) = v;
             }
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(xp_ready);
-
-            // h(k + 1) = 2^(g_end) h(k) + S(k); its bf16 copy goes to the buffer that
-            // C h^T(k - 1) read
-            if (!__all_sync(0xffffffffu,
-                            ptx::mbar_wait(&s_done[s], par) &&
-                                (k == 0 || ptx::mbar_wait(&inter_done[s ^ 1], ((k - 1) >> 1) & 1)))) {
+            return true;
+        };
+        if (nblk > 0 && !build_wx(0)) ok = false;
+        float gend_cur = gend_k;
+        for (int k = 0; k < nblk && ok; ++k) {
+            const int s = k & 1;
+            const uint32_t par = (k >> 1) & 1;
+            // B^T (w o x)(k) has completed: first w o x(k + 1), which lets the next
+            // S^T go to the tensor cores, then the state update
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&s_done[s], par))) {
+                ok = false;
+                break;
+            }
+            if (k + 1 < nblk && !build_wx(k + 1)) {
+                ok = false;
+                break;
+            }
+            const float gend = gend_cur;
+            gend_cur = gend_k;
+            // h(k + 1) = 2^(g_end) h(k) + S(k); its bf16 copy replaces the one
+            // C h^T(k) read
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&inter_done[s], par))) {
                 ok = false;
                 break;
             }
@@ -580,7 +637,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                         d2, hreg[16 * cb + m],
                         make_float2(__uint_as_float(sv[2 * m]), __uint_as_float(sv[2 * m + 1])));
             }
-            if (k + 1 < nblk) write_state_row(hb + ((k + 1) & 1) * 16384, r, hreg);
+            if (k + 1 < nblk) write_state_row(hb, r, hreg);
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             ptx::mbar_arrive(&st_done[s]);
@@ -602,26 +659,26 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         for (int k = 0; k < nblk; ++k) {
             const int s = k & 1;
             const uint32_t par = (k >> 1) & 1;
-            // the x tile of block k - 1 holds y(k - 1): release it once its store has read it
-            if (storer && k > 0) {
-                ptx::bulk_wait_group_read0();
-                ptx::mbar_arrive(&xfree[s ^ 1]);
-            }
-
-            // y(k) = 2^(g_i) inter + intra, written over this block's x tile (x has
-            // been consumed by w o x and L x), then stored as one tile by TMA
-            // (rows past the sequence end are clipped)
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&sc_ready[s], par) &&
+            // y(k) = 2^(g_i) inter + intra, staged in shared memory and stored as
+            // one tile by TMA (rows past the sequence end are clipped)
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&sc_ready[k & 3], (k >> 2) & 1) &&
                                              ptx::mbar_wait(&inter_done[s], par) &&
                                              ptx::mbar_wait(&intra_done[s], par))) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-            const float e_i = ex2(rec_all[kRec * s + r]);
+            const float e_i = ex2(rec_all[kRec * (k & 3) + r]);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&rec_free[k & 3]);
             const float2 e2 = make_float2(e_i, e_i);
-            uint8_t *tile = smem + SM::kX + s * 16384;
+            uint8_t *tile = smem + SM::kY;
             uint8_t *row = tile + r * 128;
+            // the staging tile is free once the store of y(k - 1) has read it
+            if (k > 0) {
+                if (storer) ptx::bulk_wait_group_read0();
+                asm volatile("bar.sync 8, 128;" ::: "memory");
+            }
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
                 uint32_t a[32], d[32];
