@@ -70,14 +70,14 @@ struct FusedParams {
 struct FusedSmem {
     static constexpr int kC = 0;          // 2 stages x 2 x [128 tokens][128 B]  C, K-major
     static constexpr int kB = 65536;      // 2 stages x 2 x [128 tokens][128 B]  B, K-major
-    static constexpr int kX = 131072;     // 2 stages x [128 tokens][128 B]      x, MN-major
-    static constexpr int kXP = 163840;    // [128 tokens][128 B]                 w o x
-    static constexpr int kHB = 180224;    // [128 n][128 B]                      bf16 state
-    static constexpr int kY = 196608;     // [128 tokens][128 B]                 y staging
+    static constexpr int kX = 131072;     // 3 slots x [128 tokens][128 B]       x, then y
+    static constexpr int kXP = 180224;    // [128 tokens][128 B]                 w o x
+    static constexpr int kHB = 196608;    // [128 n][128 B]                      bf16 state
     static constexpr int kF = 212992;     // 4 records: g, ngd, vcol [128]; gpiv [4]; g_end
     static constexpr int kNF = 4 * 392;   // four records (see kRec)
-    static constexpr int kBar = kF + ((kNF * 4 + 7) & ~7);
-    static constexpr int kNBar = 29;
+    static constexpr int kDT = kF + kNF * 4;   // [4][128] dt of the next records
+    static constexpr int kBar = kDT + 4 * 128 * 4;
+    static constexpr int kNBar = 33;
     static constexpr int kBytes = kBar + kNBar * 8 + 8;
 };
 static_assert(FusedSmem::kBytes <= 232448, "shared memory above the per-CTA limit");
@@ -175,17 +175,6 @@ __device__ __forceinline__ void l_block(const uint32_t (&v)[32], int col0, bool 
     }
 }
 
-// Loads dt for rows 32 qq + lane (qq = 0..3) of the block starting at t0
-// (0 past the end of the slab).
-__device__ __forceinline__ void load_dt4(const float *dtp, int64_t dt_sl, int64_t t0,
-                                         int64_t t_end, int lane, float (&dt)[4]) {
-#pragma unroll
-    for (int qq = 0; qq < 4; ++qq) {
-        const int64_t t = t0 + 32 * qq + lane;
-        dt[qq] = t < t_end ? __ldg(dtp + t * dt_sl) : 0.f;
-    }
-}
-
 // The cumulative-sum record of one 128-token block, computed by one warp
 // whose lane holds dt of rows 32 qq + lane: rec[0..127] = g (block-local
 // cumulative sum of A dt, log2 units), rec[128..255] = ngd = log2(dt) - g
@@ -226,15 +215,16 @@ __device__ __forceinline__ void build_record(const float (&dt)[4], float Ah, int
 }
 
 // Named barriers (0 is __syncthreads): 4 + q = the two warps of warpgroup A
-// on TMEM lane quarter q (q = 2, 3), 8 and 9 = warpgroup Y.
+// on TMEM lane quarter q (q = 2, 3), 9 = warpgroup Y.
 //
 // Block k uses stage s = k & 1 of the double buffers.  Tensor memory:
 // [128 s, +128) = C B^T, then L in its first 64 columns and the intra
 // accumulator in its last 64; [256 + 64 s, +64) = S^T; [384 + 64 s, +64) =
-// inter.  w o x, the bf16 state operand and the y staging tile have one
-// buffer each: w o x(k + 1) is written once B^T (w o x)(k) has completed, the
-// state entering block k + 1 once C h^T(k) has read the one entering block
-// k, and y(k) once the TMA store of y(k - 1) has read its tile.
+// inter.  x(k) lands in slot k mod 3 of a three-slot pool, where y(k) is
+// staged once L x(k) has read x(k); the slot is reloaded once the TMA store
+// of y(k) has read it.  w o x and the bf16 state operand have one buffer
+// each: w o x(k + 1) is written once B^T (w o x)(k) has completed, the state
+// entering block k + 1 once C h^T(k) has read the one entering block k.
 //
 // Every wait below names the phase of a barrier that cannot have advanced a
 // further phase yet: the later phase depends on work that the waiter itself
@@ -255,10 +245,11 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     }
     float *rec_all = reinterpret_cast<float *>(smem + SM::kF);   // [kNRec][kRec]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM::kBar);
-    uint64_t *full_C = bars, *full_B = bars + 2, *full_X = bars + 4, *cb_done = bars + 6,
-             *s_done = bars + 8, *inter_done = bars + 10, *intra_done = bars + 12,
-             *L_ready = bars + 14, *st_done = bars + 16, *drain_done = bars + 18,
-             *xp_ready = bars + 20, *sc_ready = bars + 21, *rec_free = bars + 25;
+    uint64_t *full_C = bars, *full_B = bars + 2, *cb_done = bars + 4, *s_done = bars + 6,
+             *inter_done = bars + 8, *intra_done = bars + 10, *L_ready = bars + 12,
+             *st_done = bars + 14, *drain_done = bars + 16, *xp_ready = bars + 18,
+             *sc_ready = bars + 19, *rec_free = bars + 23, *full_X = bars + 27,
+             *xfree = bars + 30;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + SM::kNBar);
     int *s_err = reinterpret_cast<int *>(tmem_slot + 1);
 
@@ -278,7 +269,6 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(&full_C[s], 1);
             ptx::mbar_init(&full_B[s], 1);
-            ptx::mbar_init(&full_X[s], 1);
             ptx::mbar_init(&cb_done[s], 1);
             ptx::mbar_init(&s_done[s], 1);
             ptx::mbar_init(&inter_done[s], 1);
@@ -291,6 +281,10 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         for (int i = 0; i < kNRec; ++i) {
             ptx::mbar_init(&sc_ready[i], 32);
             ptx::mbar_init(&rec_free[i], kRecReaders);
+        }
+        for (int i = 0; i < 3; ++i) {
+            ptx::mbar_init(&full_X[i], 1);
+            ptx::mbar_init(&xfree[i], 1);
         }
         *s_err = 0;
         ptx::fence_mbar_init();
@@ -328,8 +322,21 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         // Event loop, warp-uniform: lane 0 tests the barriers and issues the
         // copies, the whole warp builds the records.  Each stream goes ahead as
         // soon as its own buffer is free, so no copy waits behind another.
-        float dtn[4];
-        load_dt4(dtp, p.dt_sl, t_begin, t_end, lane, dtn);
+        // dt of record j is copied asynchronously into ring slot j & 3, four
+        // records ahead; each lane copies, and later reads, its own four rows.
+        float *dtring = reinterpret_cast<float *>(smem + SM::kDT);
+        auto fetch_dt = [&](int j) {
+            float *dst = dtring + 128 * (j & 3);
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                const int row = 32 * qq + lane;
+                const int64_t t = t_begin + int64_t(j) * 128 + row;
+                if (j < nblk && t < t_end) ptx::cp_async4(dst + row, dtp + t * p.dt_sl);
+                else dst[row] = 0.f;
+            }
+            ptx::cp_async_commit();   // one group per record, empty past the end
+        };
+        for (int j = 0; j < 4; ++j) fetch_dt(j);
         int kb = 0, kc = 0, kx = 0, kr = 0;   // next block of each stream
         uint64_t idle_since = 0;
         while (kb < nblk || kc < nblk || kx < nblk || kr < nblk) {
@@ -362,14 +369,14 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                         fired |= 2;
                     }
                 }
-                // x: read by w o x(k - 2) and L x(k - 2), issued after it
+                // x: its slot holds y(k - 3) until that tile's store has read it
                 if (kx < nblk) {
-                    const int s = kx & 1;
-                    const uint32_t pp = ((kx >> 1) - 1) & 1;
-                    if (kx < 2 || ptx::mbar_test_wait(&intra_done[s], pp)) {
+                    const int slot = kx % 3;
+                    if (kx < 3 || ptx::mbar_test_wait(&xfree[slot], ((kx / 3) - 1) & 1)) {
                         const int t0 = int(t_begin + int64_t(kx) * 128);
-                        ptx::mbar_arrive_expect_tx(&full_X[s], 16384);
-                        ptx::tma_load_4d(smem + SM::kX + s * 16384, &tm_x, &full_X[s], 0, h, t0, b);
+                        ptx::mbar_arrive_expect_tx(&full_X[slot], 16384);
+                        ptx::tma_load_4d(smem + SM::kX + slot * 16384, &tm_x, &full_X[slot], 0, h,
+                                         t0, b);
                         fired |= 4;
                     }
                 }
@@ -391,11 +398,11 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             kc += (fired >> 1) & 1;
             kx += (fired >> 2) & 1;
             if (fired & 8) {
+                ptx::cp_async_wait<3>();   // the group of record kr has landed
                 float dtv[4];
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq) dtv[qq] = dtn[qq];
-                if (kr + 1 < nblk)
-                    load_dt4(dtp, p.dt_sl, t_begin + int64_t(kr + 1) * 128, t_end, lane, dtn);
+                for (int qq = 0; qq < 4; ++qq) dtv[qq] = dtring[128 * (kr & 3) + 32 * qq + lane];
+                fetch_dt(kr + 4);
                 build_record(dtv, Ah, lane, rec_all + kRec * (kr & 3));
                 ptx::mbar_arrive(&sc_ready[kr & 3]);
                 ++kr;
@@ -462,7 +469,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                     const uint32_t par = (k_a >> 1) & 1;
                     if (ptx::mbar_test_wait(&L_ready[s], par)) {
                         ptx::tc_fence_after();
-                        const uint64_t x0 = dX + uint64_t(s * 1024);
+                        const uint64_t x0 = dX + uint64_t((k_a % 3) * 1024);
                         const uint32_t t_l = tmem + 128 * s;
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks)
@@ -571,14 +578,12 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         const uint32_t lane_off = uint32_t(32 * q) << 16;
         uint8_t *hb = smem + SM::kHB;
         uint8_t *xprow = smem + SM::kXP + r * 128;
-        // w o x(k), row r, into the single w o x buffer
         // g_end of the record consumed last, kept for that block's state update
         float gend_k = 0.f;
+        // w o x(k), row r, into the single w o x buffer
         auto build_wx = [&](int k) -> bool {
-            const int s = k & 1;
-            const uint32_t par = (k >> 1) & 1;
             if (!__all_sync(0xffffffffu, ptx::mbar_wait(&sc_ready[k & 3], (k >> 2) & 1) &&
-                                             ptx::mbar_wait(&full_X[s], par)))
+                                             ptx::mbar_wait(&full_X[k % 3], (k / 3) & 1)))
                 return false;
             const float *rec = rec_all + kRec * (k & 3);
             gend_k = rec[388];
@@ -586,7 +591,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&rec_free[k & 3]);
             const __nv_bfloat162 wb = __floats2bfloat162_rn(w, w);
-            const uint8_t *xrow = smem + SM::kX + s * 16384 + r * 128;
+            const uint8_t *xrow = smem + SM::kX + (k % 3) * 16384 + r * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const int off = (c ^ (r & 7)) << 4;   // swizzled: conflict-free per 8 rows
@@ -659,8 +664,9 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         for (int k = 0; k < nblk; ++k) {
             const int s = k & 1;
             const uint32_t par = (k >> 1) & 1;
-            // y(k) = 2^(g_i) inter + intra, staged in shared memory and stored as
-            // one tile by TMA (rows past the sequence end are clipped)
+            // y(k) = 2^(g_i) inter + intra, staged over x(k) (read by w o x and L x
+            // by now) and stored as one tile by TMA (rows past the sequence end are
+            // clipped)
             if (!__all_sync(0xffffffffu, ptx::mbar_wait(&sc_ready[k & 3], (k >> 2) & 1) &&
                                              ptx::mbar_wait(&inter_done[s], par) &&
                                              ptx::mbar_wait(&intra_done[s], par))) {
@@ -672,13 +678,8 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&rec_free[k & 3]);
             const float2 e2 = make_float2(e_i, e_i);
-            uint8_t *tile = smem + SM::kY;
+            uint8_t *tile = smem + SM::kX + (k % 3) * 16384;
             uint8_t *row = tile + r * 128;
-            // the staging tile is free once the store of y(k - 1) has read it
-            if (k > 0) {
-                if (storer) ptx::bulk_wait_group_read0();
-                asm volatile("bar.sync 8, 128;" ::: "memory");
-            }
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
                 uint32_t a[32], d[32];
@@ -708,6 +709,8 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             if (storer) {
                 ptx::tma_store_4d(&tm_y, tile, 0, h, int(t_begin + int64_t(k) * 128), b);
                 ptx::bulk_commit_group();
+                ptx::bulk_wait_group_read0();   // the slot takes x(k + 3) next
+                ptx::mbar_arrive(&xfree[k % 3]);
             }
         }
         if (storer) ptx::bulk_wait_group0();
