@@ -24,7 +24,7 @@ input values (bf16 and fp32 upcast exactly):
 * :func:`scalar_iir` -- the H = G = P = N = 1 special case, a first-order
   linear recurrence, in pure Python.
 
-Readings of the pages taken here (each also listed in the design doc):
+Readings of the pages taken here (where they are silent or contradict):
 the output uses the updated state h_t (inclusive causal mask i >= j);
 head h reads group h // (H // G); D and initial_states absent mean zero;
 a sequence length that is not a multiple of the chunk size is zero-padded
