@@ -23,6 +23,9 @@ input values (bf16 and fp32 upcast exactly):
   are the references for the four GPU stages.
 * :func:`scalar_iir` -- the H = G = P = N = 1 special case, a first-order
   linear recurrence, in pure Python.
+* :func:`ssu_step` -- one decode step (the selective state update) of
+  "Optimizing Nemotron v3 Super in TensorRT-LLM", section 6.1 "The SSU Math",
+  with the dt bias, softplus and z gate of section 6.2's reference, in numpy.
 
 Readings of the pages taken here (where they are silent or contradict):
 the output uses the updated state h_t (inclusive causal mask i >= j);
@@ -278,3 +281,41 @@ def scalar_iir(x, dt, a, b, c, d=0.0, s0=0.0):
         s = math.exp(a * dtt) * s + dtt * bt * xt
         ys.append(ct * s + d * xt)
     return ys, s
+
+
+def ssu_step(state, x, dt, A, Bm, Cm, D=None, z=None, dt_bias=None, dt_softplus=False,
+             ngroups=1):
+    """One decode step of the recurrence for every (batch, head), in float64.
+
+    Shapes: state [B,H,P,N], x [B,H,P], dt [B,H], A [H], Bm and Cm [B,G,N],
+    D [H], z [B,H,P], dt_bias [H].  Following the SSU math: dt' = dt (+ dt_bias),
+    softplus(dt') = log(1 + exp(dt')) when ``dt_softplus``; dA = exp(A dt');
+    new_state = state dA + dt' x (outer) B; out = new_state C + D x; out is
+    multiplied by silu(z) = z / (1 + exp(-z)) when z is given.  Head h reads
+    group h // (H // G).  Returns ``(out [B,H,P], new_state [B,H,P,N])``.
+    """
+    f = lambda t: None if t is None else np.asarray(_as_cpu(t).to(torch.float64).numpy(),
+                                                   dtype=np.float64)
+    st, xv, dtv, Av, Bv, Cv, Dv, zv, bv = (f(t) for t in (state, x, dt, A, Bm, Cm, D, z,
+                                                         dt_bias))
+    Bn, H, P, N = st.shape
+    if H % ngroups:
+        raise ValueError("oracle: nheads must be a multiple of ngroups")
+    hpg = H // ngroups
+    out = np.empty((Bn, H, P), dtype=np.float64)
+    new = np.empty_like(st)
+    for b in range(Bn):
+        for h in range(H):
+            g = h // hpg
+            d = dtv[b, h] + (bv[h] if bv is not None else 0.0)
+            if dt_softplus:
+                d = np.logaddexp(0.0, d)          # log(1 + e^d)
+            dA = math.exp(Av[h] * d)
+            new[b, h] = st[b, h] * dA + d * np.outer(xv[b, h], Bv[b, g])
+            o = new[b, h] @ Cv[b, g]
+            if Dv is not None:
+                o = o + Dv[h] * xv[b, h]
+            if zv is not None:
+                o = o * (zv[b, h] / (1.0 + np.exp(-zv[b, h])))
+            out[b, h] = o
+    return out, new
