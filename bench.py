@@ -278,12 +278,86 @@ def cpu_baseline(w, inp):
                       f"({dt:.1f} s wall)"}
 
 
+SSU_METRIC = "SSU decode tokens/s at the Nemotron hybrid layer shape; % of HBM roofline"
+
+
+def ssu_bytes(Bn, H, P, N, G):
+    """Compulsory HBM bytes of one decode step: the fp32 state read and written,
+    x, z and out (bf16), B and C (bf16), dt (f32), and A, D, dt_bias (f32)."""
+    return 2 * Bn * H * P * N * 4 + 3 * Bn * H * P * 2 + 2 * Bn * G * N * 2 + Bn * H * 4 \
+        + 3 * H * 4
+
+
+def run_ssu(args, world, rank, local):
+    """One decode step (ssd_state_update) per timed iteration, state updated in
+    place (so the state carried from step to step is real)."""
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the CUDA path has no CPU fallback)")
+    from state_space_model_gb300 import build, ssd
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    sh = dict(gen.SSU_SHAPE)
+    if args.batch is not None:
+        sh["batch"] = args.batch
+    Bn, H, P, N, G = sh["batch"], sh["nheads"], sh["headdim"], sh["dstate"], sh["ngroups"]
+    cpu = gen.make_ssu_inputs(Bn, H, P, N, G, seed=20270 + rank)
+    d = {k: (None if v is None else v.to(dev)) for k, v in cpu.items()}
+    out = torch.empty((Bn, H, P), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        ssd.state_update(d["state"], d["x"], d["dt"], d["A"], d["B"], d["C"], D=d["D"],
+                         z=d["z"], dt_bias=d["dt_bias"], dt_softplus=True, ngroups=G, out=out)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark_on()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_off()
+    barrier(world)
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
+    clk = clocks.stop()
+    pk = peaks()
+    nbytes = ssu_bytes(Bn, H, P, N, G)
+    achieved = nbytes / (ms / 1e3) / 1e9
+    if rank == 0:
+        line = {
+            "metric": SSU_METRIC, "value": world * Bn / (ms / 1e3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; see state_space_model_gb300/inputs.py)",
+            "config": {"workload": "ssu_decode", "batch": Bn, "nheads": H, "headdim": P,
+                       "dstate": N, "ngroups": G, "gated": True, "dt_softplus": True,
+                       "l2": f"state {Bn * H * P * N * 4 / 1e6:.0f} MB, larger than L2"
+                       if Bn * H * P * N * 4 > L2_BYTES else "state smaller than L2"},
+            "roofline": {"bound": "hbm", "kernel": "k_ssu_step", "achieved": achieved,
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                         "traffic": None, "algorithmic_bytes": nbytes, "kernel_ms": ms,
+                         "peak_source": pk["source"]},
+            "gpu_launches": args.steps, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--op", choices=["prefill", "ssu"], default="prefill",
+                    help="prefill: ssd_chunked_fwd (the headline); ssu: one decode step")
     ap.add_argument("--workload", default=gen.HEADLINE, choices=sorted(gen.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -300,6 +374,12 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, w, world, rank)
+        return
+    if args.op == "ssu":
+        run_ssu(args, world, rank, local)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
         return
 
     if not torch.cuda.is_available():

@@ -153,6 +153,40 @@ ssd_status ssd_chunked_fwd_static_scratch(const ssd_tensor *x, const ssd_tensor 
                                           ssd_tensor *y, ssd_tensor *final_states,
                                           void *stream);
 
+/* ---- decode step ------------------------------------------------------------ */
+
+/* One decode token of the layer: the selective state update of "Optimizing
+ * Nemotron v3 Super in TensorRT-LLM", section 6.1 "The SSU Math", with the
+ * dt bias, softplus and z gate of section 6.2's reference.  For every
+ * (b, h), with g = h / (H / G):
+ *
+ *   dt'  = dt[b, h] + dt_bias[h]                    (dt_bias optional, absent = 0)
+ *   dt'  = log(1 + exp(dt'))                        (if dt_softplus; dt' above 20
+ *                                                    is kept as is, the same in fp32)
+ *   state[b, h] = exp(A[h] dt') state[b, h] + dt' x[b, h] (outer) B[b, g]
+ *   out[b, h, p] = sum_n state[b, h, p, n] C[b, g, n] + D[h] x[b, h, p]
+ *   out *= silu(z[b, h]) = z / (1 + exp(-z))        (if z is given)
+ *
+ * Shapes, dtypes and layouts:
+ *   state [B, H, P, N] f32, packed, read and updated in place
+ *   x     [B, H, P] bf16 or f32                  z   [B, H, P] dtype of x, optional
+ *   dt    [B, H] f32 (post-softplus unless dt_softplus, then raw)
+ *   A     [H] f32 (<= 0)                         D, dt_bias [H] f32, optional
+ *   B, C  [B, G, N] dtype of x, same strides     out [B, H, P] dtype of x
+ * The state is the one ssd_chunked_fwd returns as final_states, so prefill
+ * followed by decode steps continues the same recurrence.  P and N in
+ * {16, 32, 64, 128}; H a multiple of G.  Alignment: state, B and C base
+ * pointers 16-byte aligned, B and C outer strides multiples of 16 bytes.
+ * Aliasing: out must not overlap any input or the state, and the state must
+ * not overlap any input.  Errors, ownership and streams as above; the state
+ * is modified only if the call returns SSD_OK (nothing is launched on error).
+ * One launch, no workspace. */
+ssd_status ssd_state_update(ssd_tensor *state, const ssd_tensor *x, const ssd_tensor *dt,
+                            const ssd_tensor *A, const ssd_tensor *B, const ssd_tensor *C,
+                            const ssd_tensor *D, const ssd_tensor *z,
+                            const ssd_tensor *dt_bias, int32_t dt_softplus,
+                            int64_t ngroups, ssd_tensor *out, void *stream);
+
 /* ---- stage entry points (the four steps of ssd_chunked_fwd, one call each;
  *      same conventions; used to check each step on its own) ---------------- */
 

@@ -45,6 +45,7 @@ SIGNATURES = {
     "ssd_chunked_fwd": [_T, _T, _T, _T, _T, _T, _T, _I64, _I64, _T, _T, _VP, _SZ, _VP],
     "ssd_chunked_fwd_static_scratch": [_T, _T, _T, _T, _T, _T, _T, _I64, _I64, _T, _T, _VP],
     "ssd_device_status": [_VP],
+    "ssd_state_update": [_T, _T, _T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _VP],
     "ssd_stage_chunk_cumsum": [_T, _T, _I64, _T, _VP],
     "ssd_stage_chunk_state": [_T, _T, _T, _T, _I64, _I64, _T, _VP],
     "ssd_stage_state_passing": [_T, _T, _T, _I64, _T, _T, _VP],

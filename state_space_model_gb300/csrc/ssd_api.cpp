@@ -424,6 +424,94 @@ ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt, const ssd_
     return ok();
 }
 
+ssd_status ssd_state_update(ssd_tensor *state, const ssd_tensor *x, const ssd_tensor *dt,
+                            const ssd_tensor *A, const ssd_tensor *Bm, const ssd_tensor *Cm,
+                            const ssd_tensor *D, const ssd_tensor *z, const ssd_tensor *dt_bias,
+                            int32_t dt_softplus, int64_t ngroups, ssd_tensor *out, void *stream) {
+    if (!state) return fail(SSD_ERR_INVALID_ARG, "state: null tensor descriptor");
+    if (state->ndim != 4) return fail(SSD_ERR_INVALID_ARG, "state: ndim %d, expected 4",
+                                      state->ndim);
+    if (!x) return fail(SSD_ERR_INVALID_ARG, "x: null tensor descriptor");
+    const int64_t Bn = state->shape[0], H = state->shape[1], P = state->shape[2],
+                  N = state->shape[3], G = ngroups;
+    if (Bn < 0) return fail(SSD_ERR_INVALID_ARG, "batch %lld negative", (long long)Bn);
+    if (H <= 0 || G <= 0) return fail(SSD_ERR_INVALID_ARG, "nheads %lld / ngroups %lld must be "
+                                      "positive", (long long)H, (long long)G);
+    if (H % G) return fail(SSD_ERR_INVALID_ARG, "nheads %lld is not a multiple of ngroups %lld",
+                           (long long)H, (long long)G);
+    if (!supported_dim(P))
+        return fail(SSD_ERR_UNSUPPORTED, "headdim %lld unsupported (16, 32, 64 or 128)",
+                    (long long)P);
+    if (!supported_dim(N))
+        return fail(SSD_ERR_UNSUPPORTED, "dstate %lld unsupported (16, 32, 64 or 128)",
+                    (long long)N);
+    if (Bn > 65535 || H > 65535)
+        return fail(SSD_ERR_UNSUPPORTED, "batch %lld or nheads %lld above 65535", (long long)Bn,
+                    (long long)H);
+    const int xdt = x->dtype;
+    const int64_t sst[4] = {Bn, H, P, N}, sx[3] = {Bn, H, P}, sdt[2] = {Bn, H}, sh[1] = {H},
+                  sbc[3] = {Bn, G, N};
+    ssd_status st;
+    if ((st = check_tensor(state, "state", 4, sst, SSD_F32, true, true))) return st;
+    if ((st = check_tensor(x, "x", 3, sx, -1, false, false))) return st;
+    if ((st = check_tensor(dt, "dt", 2, sdt, SSD_F32, false, false))) return st;
+    if ((st = check_tensor(A, "A", 1, sh, SSD_F32, true, false))) return st;
+    if ((st = check_tensor(Bm, "B", 3, sbc, xdt, false, true))) return st;
+    if ((st = check_tensor(Cm, "C", 3, sbc, xdt, false, true))) return st;
+    if (Bm->stride[0] != Cm->stride[0] || Bm->stride[1] != Cm->stride[1])
+        return fail(SSD_ERR_INVALID_ARG, "B and C must have the same strides");
+    if (D && (st = check_tensor(D, "D", 1, sh, SSD_F32, true, false))) return st;
+    if (z && (st = check_tensor(z, "z", 3, sx, xdt, false, false))) return st;
+    if (dt_bias && (st = check_tensor(dt_bias, "dt_bias", 1, sh, SSD_F32, true, false))) return st;
+    if ((st = check_tensor(out, "out", 3, sx, xdt, false, false))) return st;
+
+    const Range ins[] = {range_of(x), range_of(dt), range_of(A), range_of(Bm), range_of(Cm),
+                         range_of(D), range_of(z), range_of(dt_bias)};
+    const char *in_names[] = {"x", "dt", "A", "B", "C", "D", "z", "dt_bias"};
+    const Range rs = range_of(state), ro = range_of(out);
+    for (int i = 0; i < 8; ++i) {
+        if (overlap(ro, ins[i])) return fail(SSD_ERR_INVALID_ARG, "out overlaps %s", in_names[i]);
+        if (overlap(rs, ins[i]))
+            return fail(SSD_ERR_INVALID_ARG, "state overlaps %s", in_names[i]);
+    }
+    if (overlap(ro, rs)) return fail(SSD_ERR_INVALID_ARG, "out overlaps state");
+    if (Bn == 0) return ok();
+    auto dp = [](const ssd_tensor *t) -> const void * { return t ? t->data : nullptr; };
+    if ((st = check_device_ptrs({{dp(state), "state"}, {dp(x), "x"}, {dp(dt), "dt"},
+                                 {dp(A), "A"}, {dp(Bm), "B"}, {dp(Cm), "C"}, {dp(D), "D"},
+                                 {dp(z), "z"}, {dp(dt_bias), "dt_bias"}, {dp(out), "out"}})))
+        return st;
+
+    ssd::SsuArgs a;
+    a.B = int(Bn);
+    a.H = int(H);
+    a.P = int(P);
+    a.N = int(N);
+    a.G = int(G);
+    a.xdt = xdt;
+    a.softplus = dt_softplus ? 1 : 0;
+    a.state = static_cast<float *>(state->data);
+    a.x = x->data;
+    a.x_sb = x->stride[0];
+    a.x_sh = x->stride[1];
+    a.dt = static_cast<const float *>(dt->data);
+    a.dt_sb = dt->stride[0];
+    a.A = static_cast<const float *>(A->data);
+    a.D = D ? static_cast<const float *>(D->data) : nullptr;
+    a.dt_bias = dt_bias ? static_cast<const float *>(dt_bias->data) : nullptr;
+    a.Bm = Bm->data;
+    a.Cm = Cm->data;
+    a.bc_sb = Bm->stride[0];
+    a.bc_sg = Bm->stride[1];
+    a.z = z ? z->data : nullptr;
+    a.z_sb = z ? z->stride[0] : 0;
+    a.z_sh = z ? z->stride[1] : 0;
+    a.out = out->data;
+    a.o_sb = out->stride[0];
+    a.o_sh = out->stride[1];
+    return cuda_status(ssd::launch_ssu(a, static_cast<cudaStream_t>(stream)), "state update");
+}
+
 ssd_status ssd_stage_chunk_cumsum(const ssd_tensor *dt, const ssd_tensor *A, int64_t chunk_size,
                                   ssd_tensor *G, void *stream) {
     if (!dt) return fail(SSD_ERR_INVALID_ARG, "dt: null tensor descriptor");

@@ -41,6 +41,25 @@ struct Args {
     int hprev_dt = DT_F32;
 };
 
+// One decode step (ssd_state_update): strides in elements; state is packed
+// [B, H, P, N] f32; x, z, out [B, H, P]; dt [B, H]; B, C [B, G, N].
+struct SsuArgs {
+    int B = 0, H = 0, P = 0, N = 0, G = 1;
+    int xdt = DT_BF16;                        // dtype of x, B, C, z, out
+    int softplus = 0;
+    float *state = nullptr;
+    const void *x = nullptr;   int64_t x_sb = 0, x_sh = 0;
+    const float *dt = nullptr; int64_t dt_sb = 0;
+    const float *A = nullptr;
+    const float *D = nullptr;                 // may be null (= 0)
+    const float *dt_bias = nullptr;           // may be null (= 0)
+    const void *Bm = nullptr;
+    const void *Cm = nullptr;  int64_t bc_sb = 0, bc_sg = 0;   // B and C share strides
+    const void *z = nullptr;   int64_t z_sb = 0, z_sh = 0;     // may be null (no gate)
+    void *out = nullptr;       int64_t o_sb = 0, o_sh = 0;
+};
+cudaError_t launch_ssu(const SsuArgs &a, cudaStream_t stream);
+
 // Records the text ssd_last_error_detail() returns on this thread.
 void set_error_detail(const char *fmt, ...);
 

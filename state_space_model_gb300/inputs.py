@@ -105,3 +105,30 @@ def small_case(dtype="bf16", batch=2, seqlen=600, nheads=4, headdim=64,
                     ngroups, chunk_size, dtype, dt_mu=dt_mu,
                     init_states=init_states, scale_bc=(dtype == "bf16"),
                     seed=seed)
+
+
+# Decode-step (selective state update) workload: one token per sequence for
+# a batch of sequences at the Nemotron hybrid layer shape (H = 128, P = 64,
+# N = 128, G = 8), the carried state drawn like the prefill's initial state.
+SSU_SHAPE = {"batch": 64, "nheads": 128, "headdim": 64, "dstate": 128, "ngroups": 8}
+
+
+def make_ssu_inputs(batch, nheads, headdim, dstate, ngroups, seed=20270, gated=True):
+    """Draw one decode step's inputs on the CPU: state [B,H,P,N] f32, x and z
+    [B,H,P] bf16, raw dt [B,H] (softplus is applied by the step, after
+    dt_bias), dt_bias, A, D [H] f32, B and C [B,G,N] bf16 scaled by 1/sqrt(N)."""
+    g = torch.Generator().manual_seed(seed)
+    f32 = torch.float32
+    Bn, H, P, N, G = batch, nheads, headdim, dstate, ngroups
+    state = torch.randn((Bn, H, P, N), generator=g, dtype=f32) * 0.1
+    x = torch.randn((Bn, H, P), generator=g, dtype=f32)
+    Bm = torch.randn((Bn, G, N), generator=g, dtype=f32) * (1.0 / math.sqrt(N))
+    Cm = torch.randn((Bn, G, N), generator=g, dtype=f32) * (1.0 / math.sqrt(N))
+    dt_raw = torch.randn((Bn, H), generator=g, dtype=f32) * 0.5 - 2.0
+    dt_bias = torch.randn((H,), generator=g, dtype=f32) * 0.1
+    A = -torch.exp(torch.rand((H,), generator=g, dtype=f32) * math.log(16.0))
+    D = torch.randn((H,), generator=g, dtype=f32)
+    z = torch.randn((Bn, H, P), generator=g, dtype=f32) if gated else None
+    bf = torch.bfloat16
+    return {"state": state, "x": x.to(bf), "dt": dt_raw, "dt_bias": dt_bias, "A": A,
+            "B": Bm.to(bf), "C": Cm.to(bf), "D": D, "z": None if z is None else z.to(bf)}

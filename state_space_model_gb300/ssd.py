@@ -6,7 +6,8 @@ descriptors, allocates outputs and workspace with torch on the inputs'
 device, and passes the current torch stream.
 
 Layouts: x [B,L,H,P], dt [B,L,H], A [H], B/C [B,L,G,N], D [H],
-initial_states / final_states [B,H,P,N].
+initial_states / final_states [B,H,P,N]; the decode step takes one token
+per (batch, head): x, z [B,H,P], dt [B,H], B/C [B,G,N].
 """
 from __future__ import annotations
 
@@ -120,6 +121,23 @@ def chunked_fwd_static_scratch(x, dt, A, B, C, D=None, initial_states=None, chun
 
 
 # ---- the four steps, one call each -----------------------------------------
+
+def state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
+                 ngroups=1, *, out=None):
+    """One decode token (``ssd_state_update``): updates the fp32 ``state``
+    [B,H,P,N] in place and returns ``out`` [B,H,P] (dtype of x).  x, z
+    [B,H,P]; dt [B,H]; A, D, dt_bias [H]; B, C [B,G,N]."""
+    dev = _device_of(state, x, dt, A, B, C, D, z, dt_bias, out)
+    if out is None:
+        out = torch.empty(x.shape, dtype=x.dtype, device=dev)
+    lib = _native.load()
+    _native.check(lib.ssd_state_update(_desc(state), _desc(x), _desc(dt), _desc(A), _desc(B),
+                                       _desc(C), _desc(D), _desc(z), _desc(dt_bias),
+                                       1 if dt_softplus else 0, ngroups, _desc(out),
+                                       _stream(dev)),
+                  "ssd_state_update")
+    return out
+
 
 def chunk_cumsum(dt, A, chunk_size, out=None):
     """G [B, H, nc*Q] f32: log2(e) times the in-chunk inclusive cumsum of A*dt."""

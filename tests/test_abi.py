@@ -214,3 +214,53 @@ def test_python_binding_rejects_cpu_tensors(lib):
     with pytest.raises(ValueError):
         ssd.chunked_fwd(x, torch.zeros(1, 64, 2), torch.zeros(2), torch.zeros(1, 64, 1, 128),
                         torch.zeros(1, 64, 1, 128), chunk_size=64)
+
+
+def test_state_update_error_paths(lib):
+    """ssd_state_update's host checks (fake pointers, never dereferenced)."""
+    p = ctypes.pointer
+    Bn, H, P, N, G = 2, 4, 64, 128, 2
+    base = FAKE + (1 << 33)
+    state = tens((Bn, H, P, N), F32, ptr=base)
+    x = tens((Bn, H, P), BF16, ptr=base + (1 << 24))
+    dt = tens((Bn, H), F32, ptr=base + (2 << 24))
+    A = tens((H,), F32, ptr=base + (3 << 24))
+    Bm = tens((Bn, G, N), BF16, ptr=base + (4 << 24))
+    Cm = tens((Bn, G, N), BF16, ptr=base + (5 << 24))
+    out = tens((Bn, H, P), BF16, ptr=base + (6 << 24))
+
+    def call(**kw):
+        a = dict(state=state, x=x, dt=dt, A=A, Bm=Bm, Cm=Cm, D=None, z=None, dt_bias=None,
+                 softplus=0, G=G, out=out)
+        a.update(kw)
+        q = lambda t: None if t is None else p(t)
+        return lib.ssd_state_update(q(a["state"]), q(a["x"]), q(a["dt"]), q(a["A"]),
+                                    q(a["Bm"]), q(a["Cm"]), q(a["D"]), q(a["z"]),
+                                    q(a["dt_bias"]), a["softplus"], a["G"], q(a["out"]), None)
+
+    assert call(state=None) == 1 and "state" in detail(lib)
+    assert call(x=None) == 1 and "x" in detail(lib)
+    assert call(G=3) == 1 and "ngroups" in detail(lib)
+    assert call(state=tens((Bn, H, 48, N), F32, ptr=base)) == 2 and "headdim" in detail(lib)
+    assert call(state=tens((Bn, H, P, 256), F32, ptr=base)) == 2 and "dstate" in detail(lib)
+    assert call(state=tens((Bn, H, P, N), BF16, ptr=base)) == 1 and "dtype" in detail(lib)
+    assert call(dt=tens((Bn, H + 1), F32, ptr=dt.data)) == 1 and "shape" in detail(lib)
+    assert call(Cm=tens((Bn, G, N), F32, ptr=Cm.data)) == 1
+    # non-contiguous state, misaligned B
+    assert call(state=tens((Bn, H, P, N), F32, strides=(H * P * 256, P * 256, 256, 1),
+                           ptr=base)) == 1 and "contiguous" in detail(lib)
+    assert call(Bm=tens((Bn, G, N), BF16, ptr=Bm.data + 2)) == 3
+    # B and C with different strides
+    assert call(Cm=tens((Bn, G, N), BF16, strides=(G * N * 2, N * 2, 1), ptr=Cm.data)) == 1
+    assert "same strides" in detail(lib)
+    # aliasing: out over x, state over B
+    assert call(out=tens((Bn, H, P), BF16, ptr=x.data)) == 1 and "overlaps" in detail(lib)
+    assert call(Bm=tens((Bn, G, N), BF16, ptr=base)) == 1 and "overlaps" in detail(lib)
+    # optional tensors are checked when given
+    assert call(z=tens((Bn, H, P + 1), BF16, ptr=base + (7 << 24))) == 1 and "z" in detail(lib)
+    assert call(dt_bias=tens((H,), BF16, ptr=base + (8 << 24))) == 1
+    # an empty batch is valid and launches nothing
+    e0 = tens((0, H, P, N), F32, ptr=base)
+    assert call(state=e0, x=tens((0, H, P), BF16, ptr=x.data), dt=tens((0, H), F32, ptr=dt.data),
+                Bm=tens((0, G, N), BF16, ptr=Bm.data), Cm=tens((0, G, N), BF16, ptr=Cm.data),
+                out=tens((0, H, P), BF16, ptr=out.data)) == 0
