@@ -89,11 +89,16 @@ const char *ssd_last_error_detail(void);
 ssd_status ssd_device_status(void *stream);
 
 /* Bytes of device workspace ssd_chunked_fwd needs for this problem, written
- * to *bytes.  x_dtype is the ssd_dtype of x, B, C.  The workspace holds the
- * scaled in-chunk cumulative sums G [B, H, nc*Q] f32, the per-chunk states
- * [B, nc, H, P, N] f32 and the chunk-entering states [B, nc, H, P, N] in the
- * dtype of x.  Returns SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED for shapes
- * ssd_chunked_fwd would reject. */
+ * to *bytes.  x_dtype is the ssd_dtype of x, B, C.  On the four-step path the
+ * workspace holds the scaled in-chunk cumulative sums G [B, H, nc*Q] f32, the
+ * per-chunk states [B, nc, H, P, N] f32 and the chunk-entering states
+ * [B, nc, H, P, N] in the dtype of x.  The fused path needs none, except when
+ * there are fewer (batch, head) slabs than SMs and it splits them by
+ * sequence: then it holds each segment's local state, decay and entering
+ * state (at most 64 MiB; ssd_describe_plan names the split).  The answer
+ * depends on the SM count of the current device.  Returns
+ * SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED for shapes ssd_chunked_fwd would
+ * reject. */
 ssd_status ssd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads,
                               int64_t headdim, int64_t dstate, int64_t ngroups,
                               int64_t chunk_size, int32_t x_dtype,

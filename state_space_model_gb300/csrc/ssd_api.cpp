@@ -140,8 +140,8 @@ ssd_status check_geometry(int64_t B, int64_t L, int64_t H, int64_t P, int64_t N,
     return SSD_OK;
 }
 
-// Either the fused single-kernel path (no workspace) or the four-step path
-// with its intermediates in the workspace.
+// Either the fused path (workspace only for a split last wave) or the
+// four-step path with its intermediates in the workspace.
 struct Plan {
     bool fused;
     size_t off_G, off_S, off_hp, total;
@@ -150,7 +150,11 @@ struct Plan {
 Plan plan_workspace(const ssd::Dims &d, int xdt) {
     Plan p{};
     p.fused = ssd::use_fused(d, xdt);
-    if (p.fused) return p;
+    if (p.fused) {
+        // only a split last wave needs scratch (the tail segments' states)
+        p.total = ssd::fused_split(d, ssd::device_sm_count()).ws_bytes;
+        return p;
+    }
     const size_t g = size_t(d.B) * d.H * d.nc * d.Q * 4;
     const size_t s = size_t(d.B) * d.nc * d.H * d.P * d.N * 4;
     const size_t hp = size_t(d.B) * d.nc * d.H * d.P * d.N * elem_size(xdt);
@@ -279,12 +283,21 @@ const char *ssd_describe_plan(int64_t batch, int64_t seqlen, int64_t nheads, int
     a.d = d;
     a.xdt = x_dtype;
     a.hprev_dt = x_dtype;
-    char buf[256];
+    char buf[384];
     if (ssd::use_fused(d, x_dtype)) {
-        snprintf(buf, sizeof buf,
-                 "fused: k_ssd_fused x %lld CTAs ((batch, head) slabs), 128-token blocks, "
-                 "tcgen05 + TMA, no workspace",
-                 (long long)(batch * nheads));
+        const ssd::FusedSplit f = ssd::fused_split(d, ssd::device_sm_count());
+        if (f.nseg > 1)
+            snprintf(buf, sizeof buf,
+                     "fused: k_ssd_fused x %lld CTAs (%lld whole (batch, head) slabs + the last "
+                     "%lld slabs in %d segments of %lld tokens, after a states-only pass and a "
+                     "combine), 128-token blocks, tcgen05 + TMA, workspace %zu bytes",
+                     (long long)(f.n_whole + f.tail * f.nseg), (long long)f.n_whole,
+                     (long long)f.tail, f.nseg, (long long)f.seg_len, f.ws_bytes);
+        else
+            snprintf(buf, sizeof buf,
+                     "fused: k_ssd_fused x %lld CTAs ((batch, head) slabs), 128-token blocks, "
+                     "tcgen05 + TMA, no workspace",
+                     (long long)(batch * nheads));
     } else {
         snprintf(buf, sizeof buf,
                  "staged: chunk_cumsum simt, chunk_state %s, state_passing simt, chunk_scan %s",
@@ -409,6 +422,7 @@ ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt, const ssd_
     a.S = reinterpret_cast<float *>(ws + plan.off_S);
     a.h_prev = ws + plan.off_hp;
     a.hprev_dt = xdt;
+    a.ws = ws;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (plan.fused) {

@@ -44,24 +44,45 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+
 namespace ssd {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Work units.  Slabs (batch, head) are numbered heads fastest.  Slabs
+// [0, n_whole) are one unit each, walked over the whole sequence; each later
+// ("tail") slab is split into nseg segments of seg_len tokens (a multiple of
+// 128; the last one may be shorter), one unit each, so the last partial wave
+// of slabs spreads over more SMs.  A tail segment s > 0 starts from the state
+// seg_hin[tail slab][s] (computed beforehand by the states-only pass and
+// the combine kernel).  In the states-only pass (kMode 2) the units
+// are segments 0 .. nseg - 2 of every tail slab, started from zero: only
+// B^T (w o x) and the state update run, and each unit writes its final state
+// to seg_state and the sum of its blocks' log2 decays to seg_decay.
 struct FusedParams {
     int64_t L;            // sequence length
-    int64_t seg_len;      // tokens per segment (multiple of 128)
+    int64_t seg_len;      // tokens per tail segment (multiple of 128)
     int B, H, hpg, nseg;
     const float *dt;
     int64_t dt_sb, dt_sl;
     const float *A;
     const float *D;       // may be null
-    const float *h_in;    // [nseg][B][H][P][N] entering state per segment, or null (= 0)
-    float *h_out;         // [B][H][P][N] state after the last segment, or null
+    const float *h0;      // [B][H][P][N] initial state, or null (= 0)
+    float *h_final;       // [B][H][P][N] final state, or null
     __nv_bfloat16 *y;
     int64_t y_sb, y_sl, y_sh;
     unsigned int *err;
+};
+
+// What only a split launch reads (kept apart so the whole-slab kernel's
+// parameters stay as small as they can).
+struct SplitParams {
+    const float *seg_hin; // [tail slabs][nseg][P][N] entering state of tail segments
+    float *seg_state;     // [tail slabs][nseg - 1][P][N] (states-only pass)
+    float *seg_decay;     // [tail slabs][nseg - 1]        (states-only pass)
+    int n_whole;
 };
 
 // Shared memory: the operand tiles first (the 128-byte swizzle pattern repeats
@@ -215,7 +236,8 @@ __device__ __forceinline__ void build_record(const float (&dt)[4], float Ah, int
 }
 
 // Named barriers (0 is __syncthreads): 4 + q = the two warps of warpgroup A
-// on TMEM lane quarter q (q = 2, 3), 9 = warpgroup Y.
+// on TMEM lane quarter q (q = 2, 3), 9 = warpgroup Y, 11 = warpgroup S (the
+// states-only pass).
 //
 // Block k uses stage s = k & 1 of the double buffers.  Tensor memory:
 // [128 s, +128) = C B^T, then L in its first 64 columns and the intra
@@ -229,10 +251,59 @@ __device__ __forceinline__ void build_record(const float (&dt)[4], float Ah, int
 // Every wait below names the phase of a barrier that cannot have advanced a
 // further phase yet: the later phase depends on work that the waiter itself
 // enables.
+// kMode: 0 = every unit a whole slab, 1 = whole slabs then tail segments,
+// 2 = the states-only pass over tail segments.  The unit is blockIdx.x.
+template <int kMode>
+__device__ __forceinline__ void unit_range(const FusedParams &p, const SplitParams &sp,
+                                           size_t &slab, int64_t &t_begin, int64_t &t_end) {
+    const int unit = blockIdx.x;
+    int sg = 0;
+    if (kMode == 1 && unit < sp.n_whole) {
+        slab = size_t(unit);
+        t_begin = 0;
+        t_end = p.L;
+        return;
+    }
+    if (kMode == 2) {
+        slab = size_t(sp.n_whole) + unit / (p.nseg - 1);
+        sg = unit % (p.nseg - 1);
+    } else {
+        slab = size_t(sp.n_whole) + (unit - sp.n_whole) / p.nseg;
+        sg = (unit - sp.n_whole) % p.nseg;
+    }
+    t_begin = int64_t(sg) * p.seg_len;
+    t_end = t_begin + p.seg_len < p.L ? t_begin + p.seg_len : p.L;
+}
+
+// State entering the unit ([P][N] fp32), or null for zero.
+template <int kMode>
+__device__ __forceinline__ const float *unit_h_in(const FusedParams &p, const SplitParams &sp,
+                                                  size_t slab) {
+    constexpr size_t PN = 8192;
+    const int unit = blockIdx.x;
+    if (kMode == 2) return nullptr;
+    if (kMode == 1 && unit >= sp.n_whole && (unit - sp.n_whole) % p.nseg != 0)
+        return sp.seg_hin + size_t(unit - sp.n_whole) * PN;
+    return p.h0 ? p.h0 + slab * PN : nullptr;
+}
+
+// Where the unit's final state goes, or null.
+template <int kMode>
+__device__ __forceinline__ float *unit_h_out(const FusedParams &p, const SplitParams &sp,
+                                             size_t slab) {
+    constexpr size_t PN = 8192;
+    const int unit = blockIdx.x;
+    if (kMode == 2) return sp.seg_state + size_t(unit) * PN;
+    if (kMode == 1 && unit >= sp.n_whole && (unit - sp.n_whole) % p.nseg != p.nseg - 1)
+        return nullptr;
+    return p.h_final ? p.h_final + slab * PN : nullptr;
+}
+
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
             const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_y,
-            const FusedParams p) {
+            const FusedParams p, const SplitParams sp) {
     using SM = FusedSmem;
     constexpr uint32_t kCols = 512;
     constexpr uint32_t kIdCB = ptx::idesc_bf16_f32(128, 128, false, false);
@@ -254,16 +325,29 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     int *s_err = reinterpret_cast<int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // unit = (segment, batch, head), heads fastest so neighbouring CTAs share B, C in L2
-    const int unit = blockIdx.x;
-    const int h = unit % p.H;
-    const int b = (unit / p.H) % p.B;
-    const int seg = unit / (p.H * p.B);
+    constexpr bool states_only = kMode == 2;
+    // this unit's slab (heads fastest, so neighbouring CTAs share B, C in L2)
+    // and token range; its entering and final states are looked up where
+    // they are used, so no pointer stays live through the block loops
+    size_t slab;
+    int64_t t_begin, t_end;
+    int h, b, seg = 0;
+    if constexpr (kMode == 0) {
+        // every unit a whole slab (seg_len covers the sequence)
+        const int unit = blockIdx.x;
+        h = unit % p.H;
+        b = (unit / p.H) % p.B;
+        seg = unit / (p.H * p.B);
+        t_begin = int64_t(seg) * p.seg_len;
+        t_end = t_begin + p.seg_len < p.L ? t_begin + p.seg_len : p.L;
+        slab = size_t(b) * p.H + h;
+    } else {
+        unit_range<kMode>(p, sp, slab, t_begin, t_end);
+        h = int(slab) % p.H;
+        b = int(slab) / p.H;
+    }
     const int g = h / p.hpg;
-    const int64_t t_begin = int64_t(seg) * p.seg_len;
-    const int64_t t_end = t_begin + p.seg_len < p.L ? t_begin + p.seg_len : p.L;
     const int nblk = int((t_end - t_begin + 127) / 128);
-    const size_t slab = size_t(b) * p.H + h;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {
@@ -280,7 +364,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         ptx::mbar_init(xp_ready, 128);
         for (int i = 0; i < kNRec; ++i) {
             ptx::mbar_init(&sc_ready[i], 32);
-            ptx::mbar_init(&rec_free[i], kRecReaders);
+            ptx::mbar_init(&rec_free[i], states_only ? 4 : kRecReaders);
         }
         for (int i = 0; i < 3; ++i) {
             ptx::mbar_init(&full_X[i], 1);
@@ -301,7 +385,11 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     float2 hreg[32];   // state row n = r, headdim pairs (2m, 2m + 1)
     if (warp >= 8 && warp < 12) {
         const int r = 32 * (warp & 3) + lane;
-        const float *hin = p.h_in ? p.h_in + (size_t(seg) * p.B * p.H + slab) * 8192 : nullptr;
+        const float *hin;
+        if constexpr (kMode == 0)
+            hin = p.h0 ? p.h0 + (size_t(seg) * p.B * p.H + slab) * 8192 : nullptr;
+        else
+            hin = unit_h_in<kMode>(p, sp, slab);
 #pragma unroll
         for (int m = 0; m < 32; ++m)
             hreg[m] = hin ? make_float2(hin[(2 * m) * 128 + r], hin[(2 * m + 1) * 128 + r])
@@ -337,7 +425,8 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             ptx::cp_async_commit();   // one group per record, empty past the end
         };
         for (int j = 0; j < 4; ++j) fetch_dt(j);
-        int kb = 0, kc = 0, kx = 0, kr = 0;   // next block of each stream
+        // the states-only pass needs no C
+        int kb = 0, kc = states_only ? nblk : 0, kx = 0, kr = 0;   // next block of each stream
         uint64_t idle_since = 0;
         while (kb < nblk || kc < nblk || kx < nblk || kr < nblk) {
             int fired = 0;   // bit i: stream i issued (lane 0's decision)
@@ -346,7 +435,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 if (kb < nblk) {
                     const int s = kb & 1;
                     const uint32_t pp = ((kb >> 1) - 1) & 1;
-                    if (kb < 2 || (ptx::mbar_test_wait(&cb_done[s], pp) &&
+                    if (kb < 2 || ((states_only || ptx::mbar_test_wait(&cb_done[s], pp)) &&
                                    ptx::mbar_test_wait(&s_done[s], pp))) {
                         const int t0 = int(t_begin + int64_t(kb) * 128);
                         ptx::mbar_arrive_expect_tx(&full_B[s], 32768);
@@ -422,9 +511,11 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             const uint64_t dHB = ptx::sdesc(ptx::smem_u32(smem + SM::kHB), 16384, 1024);
             // K-major C / B over the state: K step 16 = 32 bytes, second 64-block 16 KB on
             constexpr uint32_t kKoff[8] = {0, 2, 4, 6, 1024, 1026, 1028, 1030};
-            int k_s = 0, k_in = 0, k_a = 0, k_cb = 0;   // next block of each product
+            // the states-only pass issues B^T (w o x) alone
+            const int k0 = states_only ? nblk : 0;
+            int k_s = 0, k_in = k0, k_a = k0, k_cb = k0;   // next block of each product
             uint64_t idle_since = 0;
-            while (k_in < nblk || k_a < nblk) {
+            while (states_only ? k_s < nblk : (k_in < nblk || k_a < nblk)) {
                 bool progress = false;
                 // S^T(k) = B^T (w o x): w o x written, B landed, and S^T(k - 2)
                 // absorbed into the state
@@ -508,8 +599,12 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             }
             // every product must land before tensor memory is released
             const int kl = nblk - 1;
-            if (ok && !ptx::mbar_wait(&intra_done[kl & 1], (kl >> 1) & 1)) ok = false;
-            if (ok && !ptx::mbar_wait(&inter_done[kl & 1], (kl >> 1) & 1)) ok = false;
+            if constexpr (states_only) {
+                if (ok && !ptx::mbar_wait(&s_done[kl & 1], (kl >> 1) & 1)) ok = false;
+            } else {
+                if (ok && !ptx::mbar_wait(&intra_done[kl & 1], (kl >> 1) & 1)) ok = false;
+                if (ok && !ptx::mbar_wait(&inter_done[kl & 1], (kl >> 1) & 1)) ok = false;
+            }
         }
     } else if (warp < 8) {
         // ---------------- warpgroup A: the decay operand ----------------
@@ -529,7 +624,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         const int r = 32 * q + lane;
         const uint32_t lane_off = uint32_t(32 * q) << 16;
         const float Dh = p.D ? p.D[h] : 0.f;
-        for (int k = 0; k < nblk; ++k) {
+        for (int k = 0; k < (states_only ? 0 : nblk); ++k) {
             const int s = k & 1;
             const uint32_t par = (k >> 1) & 1;
             if (!__all_sync(0xffffffffu, ptx::mbar_wait(&sc_ready[k & 3], (k >> 2) & 1) &&
@@ -603,10 +698,15 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             }
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(xp_ready);
+            if constexpr (states_only) {   // x(k) has no other reader: release its slot
+                asm volatile("bar.sync 11, 128;" ::: "memory");
+                if (warp == 8 && lane == 0) ptx::mbar_arrive(&xfree[k % 3]);
+            }
             return true;
         };
         if (nblk > 0 && !build_wx(0)) ok = false;
         float gend_cur = gend_k;
+        [[maybe_unused]] float gsum = 0.f;   // log2 decay of the whole unit (states-only pass)
         for (int k = 0; k < nblk && ok; ++k) {
             const int s = k & 1;
             const uint32_t par = (k >> 1) & 1;
@@ -622,11 +722,14 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             }
             const float gend = gend_cur;
             gend_cur = gend_k;
+            if constexpr (states_only) gsum += gend;
             // h(k + 1) = 2^(g_end) h(k) + S(k); its bf16 copy replaces the one
             // C h^T(k) read
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&inter_done[s], par))) {
-                ok = false;
-                break;
+            if constexpr (!states_only) {
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait(&inter_done[s], par))) {
+                    ok = false;
+                    break;
+                }
             }
             ptx::tc_fence_after();
             const float dend = ex2(gend);
@@ -642,18 +745,27 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                         d2, hreg[16 * cb + m],
                         make_float2(__uint_as_float(sv[2 * m]), __uint_as_float(sv[2 * m + 1])));
             }
-            if (k + 1 < nblk) write_state_row(hb, r, hreg);
+            if constexpr (!states_only) {
+                if (k + 1 < nblk) write_state_row(hb, r, hreg);
+            }
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             ptx::mbar_arrive(&st_done[s]);
         }
-        if (ok && p.h_out) {
-            float *ho = p.h_out + slab * 8192;
+        float *hout;
+        if constexpr (kMode == 0)
+            hout = p.h_final ? p.h_final + slab * 8192 : nullptr;
+        else
+            hout = unit_h_out<kMode>(p, sp, slab);
+        if (ok && hout) {
 #pragma unroll
             for (int m = 0; m < 32; ++m) {
-                ho[(2 * m) * 128 + r] = hreg[m].x;
-                ho[(2 * m + 1) * 128 + r] = hreg[m].y;
+                hout[(2 * m) * 128 + r] = hreg[m].x;
+                hout[(2 * m + 1) * 128 + r] = hreg[m].y;
             }
+        }
+        if constexpr (states_only) {
+            if (ok && warp == 8 && lane == 0) sp.seg_decay[blockIdx.x] = gsum;
         }
     } else {
         // ---------------- warpgroup Y: y and its TMA store ----------------
@@ -661,7 +773,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         const int r = 32 * q + lane;
         const uint32_t lane_off = uint32_t(32 * q) << 16;
         const bool storer = (warp == 12 && lane == 0);
-        for (int k = 0; k < nblk; ++k) {
+        for (int k = 0; k < (states_only ? 0 : nblk); ++k) {
             const int s = k & 1;
             const uint32_t par = (k >> 1) & 1;
             // y(k) = 2^(g_i) inter + intra, staged over x(k) (read by w o x and L x
@@ -732,6 +844,93 @@ bool fused_supported(const Dims &d, int xdt) {
     return xdt == DT_BF16 && d.P == 64 && d.N == 128 && d.Q % 128 == 0;
 }
 
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 152;   // a GB300 (describing a plan without a device)
+    }
+    return n;
+}
+
+// With at least one slab per SM the run takes about (total blocks / SMs)
+// block-times whatever the order (a CTA's blocks slow down as more SMs run),
+// so splitting would only add work.  With fewer slabs than SMs, most SMs
+// would sit idle: each slab is then split by sequence into nseg segments, at
+// the price of a states-only pass over the first nseg - 1 segments (its state
+// chain takes about a full block's time per block) plus a combine and two
+// more launches (about 16 blocks), when that shortens the run.  Costs are in
+// units of one 128-token block of the fused kernel.  Splits whose workspace
+// would pass kSplitWsMax are not considered.  The general form keeps
+// n_whole whole slabs ahead of the split ones.  SSD_NO_SPLIT=1 turns it off
+// (comparisons).
+FusedSplit fused_split(const Dims &d, int sm_count) {
+    static const bool no_split = [] {
+        const char *e = std::getenv("SSD_NO_SPLIT");
+        return e && e[0] == '1';
+    }();
+    FusedSplit f{};
+    const int64_t S = d.B * d.H;
+    const int64_t nblk = (d.L + 127) / 128;
+    const int64_t M = sm_count > 0 ? sm_count : 152;
+    f.n_whole = S;
+    f.tail = 0;
+    f.nseg = 1;
+    f.seg_len = nblk * 128;
+    const int64_t full = 0, tail = S;
+    if (no_split || S >= M || nblk < 2) return f;
+    double best = double((S + M - 1) / M) * double(nblk);
+    for (int64_t ns = 2; ns <= 64 && ns <= nblk; ++ns) {
+        const int64_t bps = (nblk + ns - 1) / ns;          // blocks per segment
+        const int64_t nseg = (nblk + bps - 1) / bps;        // no empty segment
+        if (nseg < 2) continue;
+        if (size_t(tail) * size_t(2 * nseg - 1) * size_t(d.P) * d.N * 4 + size_t(tail) * nseg * 4 +
+                3 * 256 > kSplitWsMax)
+            continue;
+        const double cost = double(full / M) * double(nblk) +
+                            double((tail * nseg + M - 1) / M) * double(bps) +
+                            double((tail * (nseg - 1) + M - 1) / M) * double(bps) + 16.0;
+        if (cost < best) {
+            best = cost;
+            f.n_whole = full;
+            f.tail = tail;
+            f.nseg = int(nseg);
+            f.seg_len = bps * 128;
+        }
+    }
+    if (f.nseg > 1) {
+        const size_t PN = size_t(d.P) * d.N;
+        auto a256 = [](size_t v) { return (v + 255) & ~size_t(255); };
+        f.off_state = 0;
+        f.off_decay = a256(f.off_state + size_t(f.tail) * (f.nseg - 1) * PN * 4);
+        f.off_hin = a256(f.off_decay + size_t(f.tail) * (f.nseg - 1) * 4);
+        f.ws_bytes = a256(f.off_hin + size_t(f.tail) * f.nseg * PN * 4);
+    }
+    return f;
+}
+
+namespace {
+// Entering state of every tail segment s >= 1, from the states-only pass:
+// h_in[s + 1] = 2^(decay_s) h_in[s] + local_s, with h_in[0] the slab's initial
+// state -- the associative combine of (decay, state) pairs of "mamba-metal",
+// "The essence of selective scan", in sequence order.  grid (tail, P N / 256).
+__global__ void __launch_bounds__(256)
+k_seg_combine(const float *h0, const float *seg_state, const float *seg_decay, float *seg_hin,
+              int n_whole, int nseg) {
+    constexpr size_t PN = 8192;
+    const int ts = blockIdx.x;
+    const size_t e = size_t(blockIdx.y) * 256 + threadIdx.x;
+    const size_t slab = size_t(n_whole) + ts;
+    float hv = h0 ? h0[slab * PN + e] : 0.f;
+    for (int sg = 0; sg + 1 < nseg; ++sg) {
+        const size_t j = size_t(ts) * (nseg - 1) + sg;
+        hv = fmaf(exp2f(seg_decay[j]), hv, seg_state[j * PN + e]);
+        seg_hin[(size_t(ts) * nseg + sg + 1) * PN + e] = hv;
+    }
+}
+}  // namespace
+
 cudaError_t launch_fused(const Args &a, cudaStream_t s) {
     const Dims &d = a.d;
     CUtensorMap tm_x, tm_b, tm_c, tm_y;
@@ -749,30 +948,55 @@ cudaError_t launch_fused(const Args &a, cudaStream_t s) {
     if ((e = make_tmap_bf16(&tm_y, a.y, 4, xd, ys, box)) != cudaSuccess) return e;
     unsigned int *err = nullptr;
     if ((e = device_error_word(&err)) != cudaSuccess) return e;
+    const FusedSplit f = fused_split(d, device_sm_count());
     FusedParams p{};
+    SplitParams sp{};
     p.L = d.L;
-    p.seg_len = ((d.L + 127) / 128) * 128;
+    p.seg_len = f.seg_len;
     p.B = int(d.B);
     p.H = int(d.H);
     p.hpg = int(d.hpg());
-    p.nseg = 1;
+    sp.n_whole = int(f.n_whole);
+    p.nseg = f.nseg;
     p.dt = a.dt;
     p.dt_sb = a.dt_sb;
     p.dt_sl = a.dt_sl;
     p.A = a.A;
     p.D = a.D;
-    p.h_in = a.h0;
-    p.h_out = a.final_states;
+    p.h0 = a.h0;
+    p.h_final = a.final_states;
+    if (f.nseg > 1) {
+        sp.seg_state = reinterpret_cast<float *>(a.ws + f.off_state);
+        sp.seg_decay = reinterpret_cast<float *>(a.ws + f.off_decay);
+        sp.seg_hin = reinterpret_cast<const float *>(a.ws + f.off_hin);
+    }
     p.y = static_cast<__nv_bfloat16 *>(a.y);
     p.y_sb = a.y_sb;
     p.y_sl = a.y_sl;
     p.y_sh = a.y_sh;
     p.err = err;
     const int smem = FusedSmem::kBytes;
-    e = cudaFuncSetAttribute(k_ssd_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const bool split = f.nseg > 1;
+    e = split ? cudaFuncSetAttribute(k_ssd_fused<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+              : cudaFuncSetAttribute(k_ssd_fused<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const unsigned units = unsigned(d.B * d.H) * unsigned(p.nseg);
-    k_ssd_fused<<<units, kThreads, smem, s>>>(tm_x, tm_b, tm_c, tm_y, p);
+    if (f.nseg > 1) {
+        // the tail segments' entering states: local states, then the combine
+        e = cudaFuncSetAttribute(k_ssd_fused<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        const unsigned pre = unsigned(f.tail) * unsigned(f.nseg - 1);
+        k_ssd_fused<2><<<pre, kThreads, smem, s>>>(tm_x, tm_b, tm_c, tm_y, p, sp);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        k_seg_combine<<<dim3(unsigned(f.tail), unsigned(d.P * d.N / 256)), 256, 0, s>>>(
+            a.h0, sp.seg_state, sp.seg_decay, reinterpret_cast<float *>(a.ws + f.off_hin),
+            sp.n_whole, f.nseg);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    const unsigned units = unsigned(f.n_whole) + unsigned(f.tail) * unsigned(f.nseg);
+    if (split)
+        k_ssd_fused<1><<<units, kThreads, smem, s>>>(tm_x, tm_b, tm_c, tm_y, p, sp);
+    else
+        k_ssd_fused<0><<<units, kThreads, smem, s>>>(tm_x, tm_b, tm_c, tm_y, p, sp);
     return cudaGetLastError();
 }
 

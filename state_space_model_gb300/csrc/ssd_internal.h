@@ -39,6 +39,7 @@ struct Args {
     float *S = nullptr;                       // [B, nc, H, P, N]
     void *h_prev = nullptr;                   // [B, nc, H, P, N]
     int hprev_dt = DT_F32;
+    char *ws = nullptr;                       // workspace base (fused path's tail split)
 };
 
 // One decode step (ssd_state_update): strides in elements; state is packed

@@ -18,6 +18,11 @@
 
 #include <mutex>
 
+#include "ssd_tc.cuh"
+
+// the fused path's split never needs more than the static array holds
+static_assert(ssd::kSplitWsMax <= SSD_STATIC_SCRATCH_BYTES, "static scratch below the split cap");
+
 namespace {
 
 // Shared by every call on a device; every GPU that loads this library holds

@@ -14,7 +14,18 @@ cudaError_t tc_chunk_scan(const Args &a, cudaStream_t s);
 
 namespace ssd {
 // The fused single-kernel forward (ssd_fused.cu): bf16, P = 64, N = 128,
-// Q a multiple of 128.  Needs no workspace.
+// Q a multiple of 128.  Needs workspace only when it splits the last wave of
+// slabs by sequence (at most kSplitWsMax bytes).
 bool fused_supported(const Dims &d, int xdt);
+// How the fused path splits the last partial wave of slabs by sequence, and
+// the workspace that needs (ws_bytes = 0 when nothing is split).
+struct FusedSplit {
+    int64_t n_whole = 0, tail = 0, seg_len = 0;
+    int nseg = 1;
+    size_t ws_bytes = 0, off_state = 0, off_decay = 0, off_hin = 0;
+};
+constexpr size_t kSplitWsMax = size_t(64) << 20;
+FusedSplit fused_split(const Dims &d, int sm_count);
+int device_sm_count();   // of the current device; 152 when there is none
 cudaError_t launch_fused(const Args &a, cudaStream_t s);
 }  // namespace ssd

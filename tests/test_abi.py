@@ -137,6 +137,36 @@ def test_describe_plan(lib):
     assert d(1, 10, 4, 64, 128, 1, 64, 9).startswith("rejected")
 
 
+def test_fused_split_plan(lib):
+    """Fewer (batch, head) slabs than SMs: the last wave is split by sequence.
+
+    The plan names the segments; the workspace holds the tail segments' local
+    states and decays and their entering states, each region 256-byte aligned.
+    A full wave or more of slabs is never split and needs no workspace.
+    """
+    import re
+    d = lambda *a: lib.ssd_describe_plan(*a).decode()
+    out = ctypes.c_size_t()
+    for B, L, H in [(1, 65536, 8), (1, 16384, 4), (1, 32768, 24), (2, 8000, 3)]:
+        plan = d(B, L, H, 64, 128, 1, 256, BF16)
+        m = re.search(r"the last (\d+) slabs in (\d+) segments of (\d+) tokens", plan)
+        assert m, plan
+        tail, nseg, seg_len = map(int, m.groups())
+        assert tail == B * H and nseg >= 2 and seg_len % 128 == 0
+        assert (nseg - 1) * seg_len < L <= nseg * seg_len
+        a256 = lambda v: (v + 255) // 256 * 256
+        PN = 64 * 128
+        ws = a256(a256(a256(tail * (nseg - 1) * PN * 4) + tail * (nseg - 1) * 4) + tail * nseg * PN * 4)
+        assert lib.ssd_workspace_size(B, L, H, 64, 128, 1, 256, BF16, ctypes.byref(out)) == 0
+        assert out.value == ws, (plan, out.value, ws)
+        assert f"workspace {ws} bytes" in plan
+    # a full wave of slabs, or one 128-token block per slab: whole slabs only
+    for B, L, H in [(8, 4096, 80), (2, 65536, 80), (1, 128, 8)]:
+        assert "segments" not in d(B, L, H, 64, 128, 1, 256, BF16)
+        assert lib.ssd_workspace_size(B, L, H, 64, 128, 1, 256, BF16, ctypes.byref(out)) == 0
+        assert out.value == 0
+
+
 def test_error_paths(lib):
     c = Case()
     # null required descriptor

@@ -332,3 +332,24 @@ def test_resume_at_chunk_boundary_is_exact(dtype):
     y2, f2 = run(w.with_(seqlen=640 - t), second)
     np.testing.assert_array_equal(np.concatenate([y1, y2], axis=1), y)
     np.testing.assert_array_equal(f2, f)
+
+
+@pytest.mark.parametrize("B,H,L,G", [(1, 4, 8000, 2), (2, 3, 5000, 1)])
+def test_fused_split_matches_oracle(B, H, L, G):
+    """Few slabs over a long sequence: each slab runs as sequence segments on
+    separate SMs, started from the combined states of a states-only pass.
+    Ragged L; initial states and D given."""
+    w = gen.small_case("bf16", batch=B, seqlen=L, nheads=H, ngroups=G, chunk_size=256,
+                       init_states=True, seed=4242 + L)
+    plan = ssd().describe_plan(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups,
+                               w.chunk_size, w.torch_dtype)
+    assert "segments" in plan, plan
+    inp = gen.make_inputs(w)
+    y, fin = run(w, inp)
+    yr, fr = oracle_full(w, inp)
+    assert rel(y, yr) <= TOL["bf16"]
+    assert rel(fin, fr) <= TOL["bf16"]
+    for b in range(B):
+        for h in range(H):
+            assert rel(y[b, :, h], yr[b, :, h]) <= TOL["bf16"]
+            assert rel(fin[b, h], fr[b, h]) <= TOL["bf16"]
