@@ -319,3 +319,45 @@ def ssu_step(state, x, dt, A, Bm, Cm, D=None, z=None, dt_bias=None, dt_softplus=
                 o = o * (zv[b, h] / (1.0 + np.exp(-zv[b, h])))
             out[b, h] = o
     return out, new
+
+
+def ssu_tokens(state, x, dt, A, Bm, Cm, D=None, z=None, dt_bias=None, dt_softplus=False,
+               ngroups=1, parent=None, update_state=True):
+    """T decode steps per sequence, in float64, as one would apply them one
+    token at a time -- the multi-token state update of "Optimizing Nemotron
+    v3 Super in TensorRT-LLM", section 10.4, with the intermediate-state cache
+    of section 10.3.
+
+    Shapes: x, z [B,T,H,P]; dt [B,T,H]; Bm, Cm [B,T,G,N]; parent [B,T]
+    integers or None.  Each sequence's running state starts at state[b]; token
+    t applies ``ssu_step`` to it, except that for t > 0 with
+    0 <= parent[b,t] < t it first restarts from the state cached after token
+    parent[b,t] (a tree of draft tokens; other values keep the chain).
+    Returns ``(out [B,T,H,P], final [B,H,P,N], cache [B,T,H,P,N])``: cache[:, t]
+    is the state after token t; final is the running state after the last
+    token, or the input state unchanged when ``update_state`` is false.
+    """
+    f = lambda t: None if t is None else _as_cpu(t).to(torch.float64)
+    st0 = f(state)
+    xv, dtv, Bv, Cv, zv = (f(t) for t in (x, dt, Bm, Cm, z))
+    Bn, T = xv.shape[0], xv.shape[1]
+    H, P, N = st0.shape[1], st0.shape[2], st0.shape[3]
+    par = None if parent is None else np.asarray(torch.as_tensor(parent).detach().cpu().numpy(),
+                                                 dtype=np.int64)
+    out = np.empty((Bn, T, H, P), dtype=np.float64)
+    cache = np.empty((Bn, T, H, P, N), dtype=np.float64)
+    final = st0.numpy().copy()
+    for b in range(Bn):
+        run = st0[b:b + 1]
+        for t in range(T):
+            if par is not None and t > 0 and 0 <= par[b, t] < t:
+                run = torch.from_numpy(cache[b:b + 1, par[b, t]].copy())
+            o, new = ssu_step(run, xv[b:b + 1, t], dtv[b:b + 1, t], A, Bv[b:b + 1, t],
+                              Cv[b:b + 1, t], D=D, z=None if zv is None else zv[b:b + 1, t],
+                              dt_bias=dt_bias, dt_softplus=dt_softplus, ngroups=ngroups)
+            out[b, t] = o[0]
+            cache[b, t] = new[0]
+            run = torch.from_numpy(new)
+        if update_state and T > 0:
+            final[b] = run[0].numpy()
+    return out, final, cache

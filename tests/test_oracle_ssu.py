@@ -172,3 +172,148 @@ def test_ssu_pins_reject_planted_mistakes(mistake):
         o, n = clean(**inp)
         np.testing.assert_allclose(o, out, rtol=1e-12, atol=1e-12)
         np.testing.assert_allclose(n, new, rtol=1e-12, atol=1e-12)
+
+
+# ---- several tokens per call (section 10.4 of the same page) ----------------
+
+def rand_token_inputs(B=2, T=6, H=4, P=3, N=5, G=2, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    r = lambda *s: torch.randn(s, generator=g, dtype=f64)
+    return dict(state=0.3 * r(B, H, P, N), x=r(B, T, H, P),
+                dt=torch.nn.functional.softplus(r(B, T, H) - 1.0),
+                A=-torch.exp(torch.rand(H, generator=g, dtype=f64) * math.log(4.0)),
+                Bm=r(B, T, G, N), Cm=r(B, T, G, N), D=r(H), ngroups=G)
+
+
+def _pred(parent_row, t):
+    """The token whose state token t starts from (-1: the call's initial state)."""
+    if t == 0:
+        return -1
+    p = int(parent_row[t])
+    return p if 0 <= p < t else t - 1
+
+
+def _path(parent_row, t):
+    path = []
+    while t >= 0:
+        path.append(t)
+        t = _pred(parent_row, t)
+    return path[::-1]
+
+
+def _recurrence_on_path(inp, b, path):
+    """The C recurrence over the tokens of `path` of sequence b: (y of the last
+    token [H,P], state after it [H,P,N])."""
+    idx = torch.tensor(path)
+    y, fin = orc.recurrence(inp["x"][b:b + 1, idx], inp["dt"][b:b + 1, idx], inp["A"],
+                            inp["Bm"][b:b + 1, idx], inp["Cm"][b:b + 1, idx], inp["D"],
+                            inp["state"][b:b + 1], ngroups=inp["ngroups"])
+    return y[0, -1], fin[0]
+
+
+def test_tokens_chain_equals_the_recurrence():
+    inp = rand_token_inputs(seed=3)
+    out, final, cache = orc.ssu_tokens(**inp)
+    y, fin = orc.recurrence(inp["x"], inp["dt"], inp["A"], inp["Bm"], inp["Cm"], inp["D"],
+                            inp["state"], ngroups=inp["ngroups"])
+    np.testing.assert_allclose(out, y, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(final, fin, rtol=1e-12, atol=1e-12)
+    T = inp["x"].shape[1]
+    for t in range(T):   # the cache holds the state after each prefix
+        _, fin_t = orc.recurrence(inp["x"][:, :t + 1], inp["dt"][:, :t + 1], inp["A"],
+                                  inp["Bm"][:, :t + 1], inp["Cm"][:, :t + 1], inp["D"],
+                                  inp["state"], ngroups=inp["ngroups"])
+        np.testing.assert_allclose(cache[:, t], fin_t, rtol=1e-12, atol=1e-12)
+
+
+TREES = [
+    [[-1, 0, 0, 1, 1, 2], [-1, -1, 0, 2, 2, 0]],     # two sequences, branching drafts
+    [[-1, 0, 1, 2, 3, 4], [-1, 0, 0, 0, 0, 0]],      # a chain and a star
+]
+
+
+@pytest.mark.parametrize("tree", TREES, ids=["branching", "chain_star"])
+def test_tokens_tree_follows_each_tokens_path(tree):
+    inp = rand_token_inputs(seed=5)
+    parent = torch.tensor(tree, dtype=torch.int32)
+    out, final, cache = orc.ssu_tokens(**inp, parent=parent)
+    B, T = parent.shape
+    for b in range(B):
+        for t in range(T):
+            y_t, st_t = _recurrence_on_path(inp, b, _path(tree[b], t))
+            np.testing.assert_allclose(out[b, t], y_t, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(cache[b, t], st_t, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(final[b], cache[b, T - 1], rtol=0, atol=0)
+
+
+def test_tokens_parent_values_outside_the_earlier_tokens_keep_the_chain():
+    inp = rand_token_inputs(seed=6)
+    chain = orc.ssu_tokens(**inp)
+    odd = torch.tensor([[5, 1, 2, 9, -3, 5], [0, 7, -1, 3, 100, -2]], dtype=torch.int32)
+    got = orc.ssu_tokens(**inp, parent=odd)
+    for a, b in zip(chain, got):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_tokens_without_state_update_leave_the_state():
+    inp = rand_token_inputs(seed=8)
+    out, final, cache = orc.ssu_tokens(**inp, update_state=False)
+    out2, final2, cache2 = orc.ssu_tokens(**inp)
+    np.testing.assert_array_equal(final, inp["state"].numpy())
+    np.testing.assert_array_equal(out, out2)
+    np.testing.assert_array_equal(cache, cache2)
+    assert not np.array_equal(final2, final)
+
+
+def _mutant_tokens(mistake):
+    """A copy of the token loop with one plausible mistake planted."""
+    def run(state, x, dt, A, Bm, Cm, D=None, ngroups=1, parent=None, update_state=True):
+        Bn, T = x.shape[0], x.shape[1]
+        out = np.empty(tuple(x.shape))
+        cache = np.empty((Bn, T) + tuple(state.shape[1:]))
+        final = state.numpy().copy()
+        for b in range(Bn):
+            run_st = state[b:b + 1]
+            for t in range(T):
+                if parent is not None and t > 0:
+                    p = int(parent[b, t])
+                    if mistake == "parent_off_by_one":
+                        p = p - 1
+                    if mistake != "parent_ignored" and 0 <= p < t:
+                        run_st = torch.from_numpy(cache[b:b + 1, p].copy())
+                o, new = orc.ssu_step(run_st, x[b:b + 1, t], dt[b:b + 1, t], A, Bm[b:b + 1, t],
+                                      Cm[b:b + 1, t], D=D, ngroups=ngroups)
+                out[b, t] = o[0]
+                cache[b, t] = run_st[0].numpy() if mistake == "cache_before_update" else new[0]
+                if mistake != "state_not_carried":
+                    run_st = torch.from_numpy(new)
+            if update_state:
+                final[b] = run_st[0].numpy()
+        return out, final, cache
+    return run
+
+
+@pytest.mark.parametrize("mistake", ["parent_off_by_one", "parent_ignored", "cache_before_update",
+                                     "state_not_carried"])
+def test_tokens_pins_reject_planted_mistakes(mistake):
+    inp = rand_token_inputs(seed=5)
+    parent = torch.tensor(TREES[0], dtype=torch.int32)
+    mut = _mutant_tokens(mistake)
+    caught = False
+    for par in (None, parent):
+        o, f, c = mut(**inp, parent=par)
+        ref = orc.ssu_tokens(**inp, parent=par)
+        # the pins above compare against the recurrence on each token's path
+        B, T = inp["x"].shape[:2]
+        for b in range(B):
+            for t in range(T):
+                row = TREES[0][b] if par is not None else [-1] * T
+                y_t, st_t = _recurrence_on_path(inp, b, _path(row, t))
+                caught |= not (np.allclose(o[b, t], y_t, rtol=1e-10) and
+                               np.allclose(c[b, t], st_t, rtol=1e-10))
+        del ref
+    assert caught, f"no pin distinguishes the mistake {mistake!r}"
+    clean = _mutant_tokens(None)
+    for par in (None, parent):
+        for a, b in zip(clean(**inp, parent=par), orc.ssu_tokens(**inp, parent=par)):
+            np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-13)
