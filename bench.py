@@ -281,16 +281,20 @@ def cpu_baseline(w, inp):
 SSU_METRIC = "SSU decode tokens/s at the Nemotron hybrid layer shape; % of HBM roofline"
 
 
-def ssu_bytes(Bn, H, P, N, G):
-    """Compulsory HBM bytes of one decode step: the fp32 state read and written,
-    x, z and out (bf16), B and C (bf16), dt (f32), and A, D, dt_bias (f32)."""
-    return 2 * Bn * H * P * N * 4 + 3 * Bn * H * P * 2 + 2 * Bn * G * N * 2 + Bn * H * 4 \
-        + 3 * H * 4
+def ssu_bytes(Bn, H, P, N, G, T=1, cached=False):
+    """Compulsory HBM bytes of one decode call of T tokens: the fp32 state read
+    and written once, the per-token state cache written when kept, and per
+    token x, z and out (bf16), B and C (bf16), dt (f32); plus A, D, dt_bias."""
+    return 2 * Bn * H * P * N * 4 + (T * Bn * H * P * N * 4 if cached else 0) + \
+        T * (3 * Bn * H * P * 2 + 2 * Bn * G * N * 2 + Bn * H * 4) + 3 * H * 4
 
 
 def run_ssu(args, world, rank, local):
-    """One decode step (ssd_state_update) per timed iteration, state updated in
-    place (so the state carried from step to step is real)."""
+    """One decode call per timed iteration, state updated in place (so the
+    state carried from step to step is real): ssd_state_update, or with
+    --tokens T > 1 ssd_state_update_tokens over T tokens per sequence keeping
+    the per-token state cache (the verification pass of speculative decoding
+    with T draft tokens)."""
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: no CUDA device (the CUDA path has no CPU fallback)")
     from state_space_model_gb300 import build, ssd
@@ -302,18 +306,41 @@ def run_ssu(args, world, rank, local):
     if args.batch is not None:
         sh["batch"] = args.batch
     Bn, H, P, N, G = sh["batch"], sh["nheads"], sh["headdim"], sh["dstate"], sh["ngroups"]
-    cpu = gen.make_ssu_inputs(Bn, H, P, N, G, seed=20270 + rank)
+    T = args.tokens
+    cpu = gen.make_ssu_inputs(Bn, H, P, N, G, seed=20270 + rank, tokens=T if T > 1 else None)
     d = {k: (None if v is None else v.to(dev)) for k, v in cpu.items()}
-    out = torch.empty((Bn, H, P), dtype=torch.bfloat16, device=dev)
+    if T > 1:
+        out = torch.empty((Bn, T, H, P), dtype=torch.bfloat16, device=dev)
+        inter = torch.empty((Bn, T, H, P, N), dtype=torch.float32, device=dev)
 
-    def step():
-        ssd.state_update(d["state"], d["x"], d["dt"], d["A"], d["B"], d["C"], D=d["D"],
-                         z=d["z"], dt_bias=d["dt_bias"], dt_softplus=True, ngroups=G, out=out)
+        def step():
+            ssd.state_update_tokens(d["state"], d["x"], d["dt"], d["A"], d["B"], d["C"],
+                                    D=d["D"], z=d["z"], dt_bias=d["dt_bias"], dt_softplus=True,
+                                    ngroups=G, intermediate_states=inter, out=out)
+    else:
+        out = torch.empty((Bn, H, P), dtype=torch.bfloat16, device=dev)
 
+        def step():
+            ssd.state_update(d["state"], d["x"], d["dt"], d["A"], d["B"], d["C"], D=d["D"],
+                             z=d["z"], dt_bias=d["dt_bias"], dt_softplus=True, ngroups=G,
+                             out=out)
+
+    # a decode step is a few microseconds of GPU work at small batch, less than
+    # the Python call that launches it: replay it from a CUDA graph, as a
+    # serving loop does, so the timed region holds GPU work and launch gaps only
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            step()
+    stream.wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
     clocks = ClockSampler(local)
     clocks.start()
     for _ in range(args.warmup):
-        step()
+        graph.replay()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
@@ -321,7 +348,7 @@ def run_ssu(args, world, rank, local):
     clocks.mark_on()
     ev0.record(stream)
     for _ in range(args.steps):
-        step()
+        graph.replay()
     ev1.record(stream)
     torch.cuda.synchronize()
     clocks.mark_off()
@@ -329,23 +356,26 @@ def run_ssu(args, world, rank, local):
     ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
     clk = clocks.stop()
     pk = peaks()
-    nbytes = ssu_bytes(Bn, H, P, N, G)
+    nbytes = ssu_bytes(Bn, H, P, N, G, T, cached=T > 1)
     achieved = nbytes / (ms / 1e3) / 1e9
     if rank == 0:
         line = {
-            "metric": SSU_METRIC, "value": world * Bn / (ms / 1e3), "unit": "tokens/s",
+            "metric": SSU_METRIC, "value": world * Bn * T / (ms / 1e3), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded; see state_space_model_gb300/inputs.py)",
-            "config": {"workload": "ssu_decode", "batch": Bn, "nheads": H, "headdim": P,
+            "config": {"workload": "ssu_decode" if T == 1 else f"ssu_decode_{T}_tokens",
+                       "batch": Bn, "tokens": T, "nheads": H, "headdim": P,
                        "dstate": N, "ngroups": G, "gated": True, "dt_softplus": True,
+                       "state_cache": T > 1,
                        "l2": f"state {Bn * H * P * N * 4 / 1e6:.0f} MB, larger than L2"
                        if Bn * H * P * N * 4 > L2_BYTES else "state smaller than L2"},
-            "roofline": {"bound": "hbm", "kernel": "k_ssu_step", "achieved": achieved,
+            "roofline": {"bound": "hbm", "kernel": "k_ssu_tokens", "achieved": achieved,
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                          "traffic": None, "algorithmic_bytes": nbytes, "kernel_ms": ms,
                          "peak_source": pk["source"]},
-            "gpu_launches": args.steps, "clocks": clk,
+            "gpu_launches": args.steps, "launch": "CUDA graph replay, one kernel per step",
+            "clocks": clk,
         }
         print(json.dumps(line), flush=True)
 
@@ -361,6 +391,9 @@ def main():
     ap.add_argument("--workload", default=gen.HEADLINE, choices=sorted(gen.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--tokens", type=int, default=1,
+                    help="--op ssu: decode tokens per sequence and call (T > 1 keeps the "
+                         "per-token state cache)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (a smaller case of the same shape)")
     ap.add_argument("--ref-seconds", type=float, default=150.0,

@@ -64,7 +64,8 @@ typedef enum {
     SSD_ERR_TIMEOUT = 6      /* a device-side bounded wait gave up           */
 } ssd_status;
 
-typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+/* SSD_I32 only for the parent indices of ssd_state_update_tokens. */
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1, SSD_I32 = 2 } ssd_dtype;
 
 typedef struct {
     void *data;          /* device pointer                                   */
@@ -191,6 +192,49 @@ ssd_status ssd_state_update(ssd_tensor *state, const ssd_tensor *x, const ssd_te
                             const ssd_tensor *D, const ssd_tensor *z,
                             const ssd_tensor *dt_bias, int32_t dt_softplus,
                             int64_t ngroups, ssd_tensor *out, void *stream);
+
+/* T decode tokens per sequence in one call, as in speculative decoding, where
+ * the draft tokens of each sequence are checked together: "Optimizing Nemotron
+ * v3 Super in TensorRT-LLM", section 10.3 "Stateful SSM Caching for
+ * Speculative Decoding" and section 10.4 "Multi-Token State Update Kernel".
+ * For every (b, h), with s the running P x N state:
+ *
+ *   s = state[b, h]
+ *   for t = 0 .. T-1:
+ *       if parent and t > 0 and 0 <= parent[b, t] < t:
+ *           s = intermediate_states[b, parent[b, t], h]     (a tree of drafts)
+ *       s = exp(A[h] dt') s + dt' x[b, t, h] (outer) B[b, t, g]   (dt' as above)
+ *       intermediate_states[b, t, h] = s                  (if given)
+ *       out[b, t, h, p] = (sum_n s[p, n] C[b, t, g, n] + D[h] x[b, t, h, p])
+ *                         * silu(z[b, t, h, p])           (z optional)
+ *   state[b, h] = s                                       (if update_state != 0)
+ *
+ * Token t starts from the state after token t - 1, unless parent[b, t] names
+ * an earlier token of the same call (0 <= parent[b, t] < t): then it starts
+ * from the state after that token.  Other parent values (-1, say) keep the
+ * chain; parent[b, 0] is not read.  With update_state = 0 the state is left
+ * as it was (a verification pass: the accepted step's intermediate state is
+ * promoted by the caller).
+ *
+ * Shapes, dtypes and layouts (the token axis second):
+ *   state [B, H, P, N] f32, packed
+ *   x, z, out [B, T, H, P] bf16 or f32 (z optional, out the dtype of x)
+ *   dt    [B, T, H] f32                          A, D, dt_bias [H] f32
+ *   B, C  [B, T, G, N] dtype of x, same strides
+ *   intermediate_states [B, T, H, P, N] f32, packed, optional (required with parent)
+ *   parent [B, T] SSD_I32, optional
+ * T = 1 without intermediate states or parents is ssd_state_update.  Alignment
+ * as for ssd_state_update, plus intermediate_states 16-byte aligned.  Aliasing:
+ * out, the state and intermediate_states overlap neither each other nor any
+ * input.  Errors, ownership and streams as above.  One launch, no workspace;
+ * the state is read and written once whatever T. */
+ssd_status ssd_state_update_tokens(ssd_tensor *state, const ssd_tensor *x, const ssd_tensor *dt,
+                                   const ssd_tensor *A, const ssd_tensor *B, const ssd_tensor *C,
+                                   const ssd_tensor *D, const ssd_tensor *z,
+                                   const ssd_tensor *dt_bias, int32_t dt_softplus,
+                                   int64_t ngroups, ssd_tensor *out,
+                                   ssd_tensor *intermediate_states, const ssd_tensor *parent,
+                                   int32_t update_state, void *stream);
 
 /* ---- stage entry points (the four steps of ssd_chunked_fwd, one call each;
  *      same conventions; used to check each step on its own) ---------------- */

@@ -12,7 +12,7 @@ import threading
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libssd_gb300.so")
 
-SSD_F32, SSD_BF16 = 0, 1
+SSD_F32, SSD_BF16, SSD_I32 = 0, 1, 2
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED",
           3: "SSD_ERR_ALIGNMENT", 4: "SSD_ERR_WORKSPACE", 5: "SSD_ERR_CUDA",
           6: "SSD_ERR_TIMEOUT"}
@@ -46,6 +46,8 @@ SIGNATURES = {
     "ssd_chunked_fwd_static_scratch": [_T, _T, _T, _T, _T, _T, _T, _I64, _I64, _T, _T, _VP],
     "ssd_device_status": [_VP],
     "ssd_state_update": [_T, _T, _T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _VP],
+    "ssd_state_update_tokens": [_T, _T, _T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _T, _T, _I32,
+                                _VP],
     "ssd_stage_chunk_cumsum": [_T, _T, _I64, _T, _VP],
     "ssd_stage_chunk_state": [_T, _T, _T, _T, _I64, _I64, _T, _VP],
     "ssd_stage_state_passing": [_T, _T, _T, _I64, _T, _T, _VP],

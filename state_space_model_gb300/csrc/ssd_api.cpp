@@ -31,7 +31,7 @@ ssd_status ok() {
     return SSD_OK;
 }
 
-size_t elem_size(int dt) { return dt == SSD_F32 ? 4 : 2; }
+size_t elem_size(int dt) { return dt == SSD_BF16 ? 2 : 4; }
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 bool supported_dim(int64_t v) { return v == 16 || v == 32 || v == 64 || v == 128; }
@@ -66,18 +66,20 @@ bool overlap(Range a, Range b) {
 }
 
 // Checks one tensor's rank, dtype, shape, unit inner stride and alignment.
-// dtype < 0 accepts f32 or bf16.  contiguous demands packed row-major strides.
+// dtype < 0 accepts f32 or bf16 (int32 only where asked for by name).
+// contiguous demands packed row-major strides.
 ssd_status check_tensor(const ssd_tensor *t, const char *name, int ndim,
                         const int64_t *shape, int dtype, bool contiguous,
                         bool align_strides16) {
     if (!t) return fail(SSD_ERR_INVALID_ARG, "%s: null tensor descriptor", name);
     if (t->ndim != ndim)
         return fail(SSD_ERR_INVALID_ARG, "%s: ndim %d, expected %d", name, t->ndim, ndim);
-    if (t->dtype != SSD_F32 && t->dtype != SSD_BF16)
+    auto dname = [](int d) { return d == SSD_F32 ? "f32" : d == SSD_BF16 ? "bf16" : "i32"; };
+    if (t->dtype != SSD_F32 && t->dtype != SSD_BF16 && t->dtype != SSD_I32)
         return fail(SSD_ERR_INVALID_ARG, "%s: unknown dtype code %d", name, t->dtype);
-    if (dtype >= 0 && t->dtype != dtype)
-        return fail(SSD_ERR_INVALID_ARG, "%s: dtype %s, expected %s", name,
-                    t->dtype == SSD_F32 ? "f32" : "bf16", dtype == SSD_F32 ? "f32" : "bf16");
+    if ((dtype >= 0 && t->dtype != dtype) || (dtype < 0 && t->dtype == SSD_I32))
+        return fail(SSD_ERR_INVALID_ARG, "%s: dtype %s, expected %s", name, dname(t->dtype),
+                    dtype >= 0 ? dname(dtype) : "f32 or bf16");
     int64_t numel = 1;
     for (int i = 0; i < ndim; ++i) {
         if (t->shape[i] != shape[i])
@@ -438,17 +440,27 @@ ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt, const ssd_
     return ok();
 }
 
-ssd_status ssd_state_update(ssd_tensor *state, const ssd_tensor *x, const ssd_tensor *dt,
-                            const ssd_tensor *A, const ssd_tensor *Bm, const ssd_tensor *Cm,
-                            const ssd_tensor *D, const ssd_tensor *z, const ssd_tensor *dt_bias,
-                            int32_t dt_softplus, int64_t ngroups, ssd_tensor *out, void *stream) {
+namespace {
+
+// ssd_state_update (tokens = false: no token axis, T = 1) and
+// ssd_state_update_tokens (tokens = true).
+ssd_status state_update_impl(bool tokens, ssd_tensor *state, const ssd_tensor *x,
+                             const ssd_tensor *dt, const ssd_tensor *A, const ssd_tensor *Bm,
+                             const ssd_tensor *Cm, const ssd_tensor *D, const ssd_tensor *z,
+                             const ssd_tensor *dt_bias, int32_t dt_softplus, int64_t ngroups,
+                             ssd_tensor *out, ssd_tensor *inter, const ssd_tensor *parent,
+                             int32_t update_state, void *stream) {
     if (!state) return fail(SSD_ERR_INVALID_ARG, "state: null tensor descriptor");
     if (state->ndim != 4) return fail(SSD_ERR_INVALID_ARG, "state: ndim %d, expected 4",
                                       state->ndim);
     if (!x) return fail(SSD_ERR_INVALID_ARG, "x: null tensor descriptor");
+    if (tokens && x->ndim != 4)
+        return fail(SSD_ERR_INVALID_ARG, "x: ndim %d, expected 4", x->ndim);
     const int64_t Bn = state->shape[0], H = state->shape[1], P = state->shape[2],
-                  N = state->shape[3], G = ngroups;
-    if (Bn < 0) return fail(SSD_ERR_INVALID_ARG, "batch %lld negative", (long long)Bn);
+                  N = state->shape[3], G = ngroups, T = tokens ? x->shape[1] : 1;
+    if (Bn < 0 || T < 0)
+        return fail(SSD_ERR_INVALID_ARG, "batch %lld / tokens %lld negative", (long long)Bn,
+                    (long long)T);
     if (H <= 0 || G <= 0) return fail(SSD_ERR_INVALID_ARG, "nheads %lld / ngroups %lld must be "
                                       "positive", (long long)H, (long long)G);
     if (H % G) return fail(SSD_ERR_INVALID_ARG, "nheads %lld is not a multiple of ngroups %lld",
@@ -459,71 +471,125 @@ ssd_status ssd_state_update(ssd_tensor *state, const ssd_tensor *x, const ssd_te
     if (!supported_dim(N))
         return fail(SSD_ERR_UNSUPPORTED, "dstate %lld unsupported (16, 32, 64 or 128)",
                     (long long)N);
-    if (Bn > 65535 || H > 65535)
-        return fail(SSD_ERR_UNSUPPORTED, "batch %lld or nheads %lld above 65535", (long long)Bn,
-                    (long long)H);
+    if (Bn > 65535 || H > 65535 || T > (int64_t(1) << 30))
+        return fail(SSD_ERR_UNSUPPORTED, "batch %lld or nheads %lld above 65535, or tokens %lld "
+                    "above 2^30", (long long)Bn, (long long)H, (long long)T);
+    if (parent && !inter)
+        return fail(SSD_ERR_INVALID_ARG, "parent needs intermediate_states (the parents' "
+                    "states are read from there)");
     const int xdt = x->dtype;
-    const int64_t sst[4] = {Bn, H, P, N}, sx[3] = {Bn, H, P}, sdt[2] = {Bn, H}, sh[1] = {H},
-                  sbc[3] = {Bn, G, N};
+    // shapes with the token axis (index 1) when `tokens`, without it otherwise
+    const int k = tokens ? 1 : 0;
+    const int64_t sst[4] = {Bn, H, P, N};
+    const int64_t sx4[4] = {Bn, T, H, P}, sx3[3] = {Bn, H, P};
+    const int64_t sdt3[3] = {Bn, T, H}, sdt2[2] = {Bn, H};
+    const int64_t sbc4[4] = {Bn, T, G, N}, sbc3[3] = {Bn, G, N};
+    const int64_t sh[1] = {H}, sin[5] = {Bn, T, H, P, N}, spar[2] = {Bn, T};
+    const int64_t *sx = tokens ? sx4 : sx3, *sdt = tokens ? sdt3 : sdt2,
+                  *sbc = tokens ? sbc4 : sbc3;
     ssd_status st;
     if ((st = check_tensor(state, "state", 4, sst, SSD_F32, true, true))) return st;
-    if ((st = check_tensor(x, "x", 3, sx, -1, false, false))) return st;
-    if ((st = check_tensor(dt, "dt", 2, sdt, SSD_F32, false, false))) return st;
+    if ((st = check_tensor(x, "x", 3 + k, sx, -1, false, false))) return st;
+    if ((st = check_tensor(dt, "dt", 2 + k, sdt, SSD_F32, false, false))) return st;
     if ((st = check_tensor(A, "A", 1, sh, SSD_F32, true, false))) return st;
-    if ((st = check_tensor(Bm, "B", 3, sbc, xdt, false, true))) return st;
-    if ((st = check_tensor(Cm, "C", 3, sbc, xdt, false, true))) return st;
-    if (Bm->stride[0] != Cm->stride[0] || Bm->stride[1] != Cm->stride[1])
-        return fail(SSD_ERR_INVALID_ARG, "B and C must have the same strides");
+    if ((st = check_tensor(Bm, "B", 3 + k, sbc, xdt, false, true))) return st;
+    if ((st = check_tensor(Cm, "C", 3 + k, sbc, xdt, false, true))) return st;
+    for (int i = 0; i < 2 + k; ++i)
+        if (Bm->stride[i] != Cm->stride[i])
+            return fail(SSD_ERR_INVALID_ARG, "B and C must have the same strides");
     if (D && (st = check_tensor(D, "D", 1, sh, SSD_F32, true, false))) return st;
-    if (z && (st = check_tensor(z, "z", 3, sx, xdt, false, false))) return st;
+    if (z && (st = check_tensor(z, "z", 3 + k, sx, xdt, false, false))) return st;
     if (dt_bias && (st = check_tensor(dt_bias, "dt_bias", 1, sh, SSD_F32, true, false))) return st;
-    if ((st = check_tensor(out, "out", 3, sx, xdt, false, false))) return st;
+    if ((st = check_tensor(out, "out", 3 + k, sx, xdt, false, false))) return st;
+    if (inter && (st = check_tensor(inter, "intermediate_states", 5, sin, SSD_F32, true, true)))
+        return st;
+    if (parent && (st = check_tensor(parent, "parent", 2, spar, SSD_I32, false, false)))
+        return st;
 
     const Range ins[] = {range_of(x), range_of(dt), range_of(A), range_of(Bm), range_of(Cm),
-                         range_of(D), range_of(z), range_of(dt_bias)};
-    const char *in_names[] = {"x", "dt", "A", "B", "C", "D", "z", "dt_bias"};
-    const Range rs = range_of(state), ro = range_of(out);
-    for (int i = 0; i < 8; ++i) {
+                         range_of(D), range_of(z), range_of(dt_bias), range_of(parent)};
+    const char *in_names[] = {"x", "dt", "A", "B", "C", "D", "z", "dt_bias", "parent"};
+    const Range rs = range_of(state), ro = range_of(out), ri = range_of(inter);
+    for (int i = 0; i < 9; ++i) {
         if (overlap(ro, ins[i])) return fail(SSD_ERR_INVALID_ARG, "out overlaps %s", in_names[i]);
         if (overlap(rs, ins[i]))
             return fail(SSD_ERR_INVALID_ARG, "state overlaps %s", in_names[i]);
+        if (overlap(ri, ins[i]))
+            return fail(SSD_ERR_INVALID_ARG, "intermediate_states overlaps %s", in_names[i]);
     }
     if (overlap(ro, rs)) return fail(SSD_ERR_INVALID_ARG, "out overlaps state");
-    if (Bn == 0) return ok();
+    if (overlap(ri, rs) || overlap(ri, ro))
+        return fail(SSD_ERR_INVALID_ARG, "intermediate_states overlaps state or out");
+    if (Bn == 0 || T == 0) return ok();
     auto dp = [](const ssd_tensor *t) -> const void * { return t ? t->data : nullptr; };
     if ((st = check_device_ptrs({{dp(state), "state"}, {dp(x), "x"}, {dp(dt), "dt"},
                                  {dp(A), "A"}, {dp(Bm), "B"}, {dp(Cm), "C"}, {dp(D), "D"},
-                                 {dp(z), "z"}, {dp(dt_bias), "dt_bias"}, {dp(out), "out"}})))
+                                 {dp(z), "z"}, {dp(dt_bias), "dt_bias"}, {dp(out), "out"},
+                                 {dp(inter), "intermediate_states"}, {dp(parent), "parent"}})))
         return st;
 
+    // stride of the token axis (0 without one) and of the axes after it
+    auto sT = [&](const ssd_tensor *t) -> int64_t { return tokens ? t->stride[1] : 0; };
+    auto sAt = [&](const ssd_tensor *t, int i) -> int64_t { return t->stride[i + k]; };
     ssd::SsuArgs a;
     a.B = int(Bn);
+    a.T = int(T);
     a.H = int(H);
     a.P = int(P);
     a.N = int(N);
     a.G = int(G);
     a.xdt = xdt;
     a.softplus = dt_softplus ? 1 : 0;
+    a.update = update_state ? 1 : 0;
     a.state = static_cast<float *>(state->data);
     a.x = x->data;
     a.x_sb = x->stride[0];
-    a.x_sh = x->stride[1];
+    a.x_st = sT(x);
+    a.x_sh = sAt(x, 1);
     a.dt = static_cast<const float *>(dt->data);
     a.dt_sb = dt->stride[0];
+    a.dt_st = sT(dt);
     a.A = static_cast<const float *>(A->data);
     a.D = D ? static_cast<const float *>(D->data) : nullptr;
     a.dt_bias = dt_bias ? static_cast<const float *>(dt_bias->data) : nullptr;
     a.Bm = Bm->data;
     a.Cm = Cm->data;
     a.bc_sb = Bm->stride[0];
-    a.bc_sg = Bm->stride[1];
+    a.bc_st = sT(Bm);
+    a.bc_sg = sAt(Bm, 1);
     a.z = z ? z->data : nullptr;
     a.z_sb = z ? z->stride[0] : 0;
-    a.z_sh = z ? z->stride[1] : 0;
+    a.z_st = z ? sT(z) : 0;
+    a.z_sh = z ? sAt(z, 1) : 0;
     a.out = out->data;
     a.o_sb = out->stride[0];
-    a.o_sh = out->stride[1];
+    a.o_st = sT(out);
+    a.o_sh = sAt(out, 1);
+    a.inter = inter ? static_cast<float *>(inter->data) : nullptr;
+    a.parent = parent ? static_cast<const int32_t *>(parent->data) : nullptr;
+    a.par_sb = parent ? parent->stride[0] : 0;
     return cuda_status(ssd::launch_ssu(a, static_cast<cudaStream_t>(stream)), "state update");
+}
+
+}  // namespace
+
+ssd_status ssd_state_update(ssd_tensor *state, const ssd_tensor *x, const ssd_tensor *dt,
+                            const ssd_tensor *A, const ssd_tensor *Bm, const ssd_tensor *Cm,
+                            const ssd_tensor *D, const ssd_tensor *z, const ssd_tensor *dt_bias,
+                            int32_t dt_softplus, int64_t ngroups, ssd_tensor *out, void *stream) {
+    return state_update_impl(false, state, x, dt, A, Bm, Cm, D, z, dt_bias, dt_softplus, ngroups,
+                             out, nullptr, nullptr, 1, stream);
+}
+
+ssd_status ssd_state_update_tokens(ssd_tensor *state, const ssd_tensor *x, const ssd_tensor *dt,
+                                   const ssd_tensor *A, const ssd_tensor *Bm,
+                                   const ssd_tensor *Cm, const ssd_tensor *D, const ssd_tensor *z,
+                                   const ssd_tensor *dt_bias, int32_t dt_softplus,
+                                   int64_t ngroups, ssd_tensor *out,
+                                   ssd_tensor *intermediate_states, const ssd_tensor *parent,
+                                   int32_t update_state, void *stream) {
+    return state_update_impl(true, state, x, dt, A, Bm, Cm, D, z, dt_bias, dt_softplus, ngroups,
+                             out, intermediate_states, parent, update_state, stream);
 }
 
 ssd_status ssd_stage_chunk_cumsum(const ssd_tensor *dt, const ssd_tensor *A, int64_t chunk_size,

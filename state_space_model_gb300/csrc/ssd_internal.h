@@ -42,22 +42,28 @@ struct Args {
     char *ws = nullptr;                       // workspace base (fused path's tail split)
 };
 
-// One decode step (ssd_state_update): strides in elements; state is packed
-// [B, H, P, N] f32; x, z, out [B, H, P]; dt [B, H]; B, C [B, G, N].
+// T decode steps per sequence (ssd_state_update_tokens; ssd_state_update is
+// T = 1): strides in elements; state is packed [B, H, P, N] f32; x, z, out
+// [B, T, H, P]; dt [B, T, H]; B, C [B, T, G, N]; intermediate states packed
+// [B, T, H, P, N] f32; parent [B, T] int32.
 struct SsuArgs {
-    int B = 0, H = 0, P = 0, N = 0, G = 1;
+    int B = 0, T = 1, H = 0, P = 0, N = 0, G = 1;
     int xdt = DT_BF16;                        // dtype of x, B, C, z, out
     int softplus = 0;
+    int update = 1;                           // write the final state back
     float *state = nullptr;
-    const void *x = nullptr;   int64_t x_sb = 0, x_sh = 0;
-    const float *dt = nullptr; int64_t dt_sb = 0;
+    const void *x = nullptr;   int64_t x_sb = 0, x_st = 0, x_sh = 0;
+    const float *dt = nullptr; int64_t dt_sb = 0, dt_st = 0;
     const float *A = nullptr;
     const float *D = nullptr;                 // may be null (= 0)
     const float *dt_bias = nullptr;           // may be null (= 0)
     const void *Bm = nullptr;
-    const void *Cm = nullptr;  int64_t bc_sb = 0, bc_sg = 0;   // B and C share strides
-    const void *z = nullptr;   int64_t z_sb = 0, z_sh = 0;     // may be null (no gate)
-    void *out = nullptr;       int64_t o_sb = 0, o_sh = 0;
+    const void *Cm = nullptr;  int64_t bc_sb = 0, bc_st = 0, bc_sg = 0;   // B, C share strides
+    const void *z = nullptr;   int64_t z_sb = 0, z_st = 0, z_sh = 0;     // may be null
+    void *out = nullptr;       int64_t o_sb = 0, o_st = 0, o_sh = 0;
+    float *inter = nullptr;                   // may be null (not cached)
+    const int32_t *parent = nullptr;          // may be null (a chain)
+    int64_t par_sb = 0;
 };
 cudaError_t launch_ssu(const SsuArgs &a, cudaStream_t stream);
 

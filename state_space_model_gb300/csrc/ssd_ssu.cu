@@ -1,18 +1,28 @@
-// Decode step of the Mamba-2 layer -- the selective state update of
+// Decode steps of the Mamba-2 layer -- the selective state update of
 // "Optimizing Nemotron v3 Super in TensorRT-LLM", section 6.1 "The SSU Math",
-// with the dt bias, softplus and z gate of section 6.2's reference:
+// with the dt bias, softplus and z gate of section 6.2's reference, applied
+// to T tokens per sequence in one launch as in section 10.4 "Multi-Token
+// State Update Kernel":
 //     dt' = softplus(dt + dt_bias)          (each step optional)
-//     state = exp(A dt') state + dt' x (outer) B        (fp32, in place)
+//     state = exp(A dt') state + dt' x (outer) B        (fp32)
 //     out   = (state C + D x) * silu(z)
-// for every (batch, head), head h reading group h / (H / G).
+// for every (batch, head), head h reading group h / (H / G); token t > 0 may
+// start from the cached state after an earlier token (its parent) instead of
+// the one after token t - 1.
 //
-// The step reads and writes the whole fp32 state once and everything else is
-// a few hundred bytes per head, so it is bound by HBM: each thread streams
-// four consecutive state columns of one row with 16-byte loads and stores
-// (a row is N / 4 contiguous lanes, coalesced), and the row's output is a
-// shuffle reduction over those lanes.  No tensor cores: the only contraction
-// is a length-N dot product per row.
+// The step reads and writes the fp32 state once per call, whatever T, and
+// everything else is a few hundred bytes per head and token, so it is bound
+// by HBM.  Each CTA owns a tile of state rows of one (batch, head): one
+// elected thread brings the whole tile into shared memory with bulk copies
+// (the bytes in flight cost no registers, so an SM keeps several tiles in
+// flight), every thread then takes four consecutive columns of its rows into
+// registers, runs the T tokens there, and writes the cached and final
+// states with coalesced 16-byte stores.  A row's output is a shuffle
+// reduction over the lanes holding it.  No tensor cores: the only
+// contraction is a length-N dot product per row.
+#include "ptx_sm100.cuh"
 #include "ssd_internal.h"
+#include "ssd_tc.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -20,7 +30,10 @@
 namespace ssd {
 namespace {
 
-constexpr int kSsuThreads = 256;
+constexpr int kSsuThreads = 128;
+constexpr int kMaxRT = 16;                 // rows per thread at most (64 fp32 registers)
+constexpr uint32_t kBulkChunk = 16384;     // bytes per bulk copy
+constexpr unsigned kErrTimeout = 1u;       // same bit as the fused forward's
 
 template <typename T>
 __device__ __forceinline__ float to_f(T v);
@@ -49,77 +62,151 @@ __device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
     return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
-// grid (ceil(P / (kRows kR)), H, B); block kSsuThreads = kRows x (N / 4)
-// threads; each thread owns four columns of kR rows kRows apart and issues
-// all kR state loads before using any, so enough bytes are in flight per SM
-// to cover the memory latency.
-constexpr int kR = 4;
-
+// grid (P / R, H, B), block kSsuThreads = kRowsPass x (N / 4) threads,
+// dynamic shared memory R N 4 bytes.  R = rows: a multiple of kRowsPass of at
+// most kMaxRT kRowsPass, or all P rows when P < kRowsPass.  Thread (rr, c)
+// owns columns 4c .. 4c + 3 of the local rows rr + i kRowsPass below R.
+// Each token's x and z values of the tile's rows are staged in shared memory
+// (double-buffered by token parity) so no row waits on its own global load.
 template <int N, typename T>
-__global__ void __launch_bounds__(kSsuThreads)
-k_ssu_step(const SsuArgs a) {
-    constexpr int kTpr = N / 4;                    // threads per state row
-    constexpr int kRows = kSsuThreads / kTpr;      // rows per pass
+__global__ void __launch_bounds__(kSsuThreads, 5)
+k_ssu_tokens(const SsuArgs a, int rows, unsigned int *err) {
+    constexpr int kTpr = N / 4;                     // threads per state row
+    constexpr int kRowsPass = kSsuThreads / kTpr;   // rows per pass
+    extern __shared__ __align__(16) float4 tile[];
+    __shared__ uint64_t full;
+    __shared__ float xs[2][128], zs[2][128];        // rows <= P <= 128
     const int b = blockIdx.z, h = blockIdx.y;
     const int g = h / (a.H / a.G);
-    const int row0 = blockIdx.x * kRows * kR + threadIdx.x / kTpr;
-    const int c0 = (threadIdx.x % kTpr) * 4;
+    const int r0 = blockIdx.x * rows;
+    const int c = threadIdx.x % kTpr, rr = threadIdx.x / kTpr;
+    const int nrt = (rows + kRowsPass - 1) / kRowsPass;   // uniform over the CTA
+    const size_t head = size_t(b) * a.H + h;
+    float *st = a.state + (head * a.P + r0) * N;
+    const uint32_t bytes = uint32_t(rows) * N * 4;
 
-    float4 s[kR];
-    float4 *sp[kR];
-    bool live[kR];
-#pragma unroll
-    for (int i = 0; i < kR; ++i) {
-        const int row = row0 + i * kRows;
-        live[i] = row < a.P;
-        sp[i] = reinterpret_cast<float4 *>(a.state + ((int64_t(b) * a.H + h) * a.P + row) * N + c0);
-        s[i] = live[i] ? *sp[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&full, 1);
+        ptx::fence_mbar_init();
     }
-    float d = a.dt[int64_t(b) * a.dt_sb + h];
-    if (a.dt_bias) d += a.dt_bias[h];
-    if (a.softplus) d = d <= 20.f ? log1pf(expf(d)) : d;   // log(1 + e^d), = d to fp32 above 20
-    const float dA = expf(a.A[h] * d);
-    const int64_t bc = int64_t(b) * a.bc_sb + int64_t(g) * a.bc_sg + c0;
-    const float4 bq = load4(static_cast<const T *>(a.Bm) + bc);
-    const float4 cq = load4(static_cast<const T *>(a.Cm) + bc);
-    const T *xr = static_cast<const T *>(a.x) + int64_t(b) * a.x_sb + int64_t(h) * a.x_sh;
-
-#pragma unroll
-    for (int i = 0; i < kR; ++i) {
-        const int row = row0 + i * kRows;
-        float partial = 0.f, xv = 0.f;
-        if (live[i]) {
-            xv = to_f(xr[row]);
-            const float u = d * xv;
-            s[i].x = fmaf(s[i].x, dA, u * bq.x);
-            s[i].y = fmaf(s[i].y, dA, u * bq.y);
-            s[i].z = fmaf(s[i].z, dA, u * bq.z);
-            s[i].w = fmaf(s[i].w, dA, u * bq.w);
-            *sp[i] = s[i];
-            partial = fmaf(s[i].x, cq.x, fmaf(s[i].y, cq.y, fmaf(s[i].z, cq.z, s[i].w * cq.w)));
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        ptx::mbar_arrive_expect_tx(&full, bytes);
+        for (uint32_t off = 0; off < bytes; off += kBulkChunk)
+            ptx::bulk_load(reinterpret_cast<char *>(tile) + off,
+                           reinterpret_cast<const char *>(st) + off,
+                           bytes - off < kBulkChunk ? bytes - off : kBulkChunk, &full);
+    }
+    const float Ah = a.A[h];
+    const float Dh = a.D ? a.D[h] : 0.f;
+    const float bias = a.dt_bias ? a.dt_bias[h] : 0.f;
+    // token t's x and z of this tile's rows into buffer t & 1
+    auto stage_xz = [&](int t) {
+        if (threadIdx.x < rows) {
+            const int row = r0 + threadIdx.x;
+            xs[t & 1][threadIdx.x] = to_f(static_cast<const T *>(a.x)[
+                int64_t(b) * a.x_sb + int64_t(t) * a.x_st + int64_t(h) * a.x_sh + row]);
+            if (a.z)
+                zs[t & 1][threadIdx.x] = to_f(static_cast<const T *>(a.z)[
+                    int64_t(b) * a.z_sb + int64_t(t) * a.z_st + int64_t(h) * a.z_sh + row]);
         }
-        // sum over the row's kTpr lanes (contiguous within the warp)
+    };
+    stage_xz(0);   // overlaps the state copy
+    if (!ptx::mbar_wait(&full, 0)) {   // uniform: every thread gives up on the same copy
+        if (threadIdx.x == 0) atomicOr(err, kErrTimeout);
+        return;
+    }
+    float4 s[kMaxRT];
 #pragma unroll
-        for (int off = kTpr / 2; off > 0; off >>= 1)
-            partial += __shfl_xor_sync(0xffffffffu, partial, off);
-        if (live[i] && threadIdx.x % kTpr == 0) {
-            float o = partial;
-            if (a.D) o = fmaf(a.D[h], xv, o);
-            if (a.z) {
-                const float zv = to_f(static_cast<const T *>(a.z)[int64_t(b) * a.z_sb +
-                                                                  int64_t(h) * a.z_sh + row]);
-                o *= zv / (1.f + expf(-zv));
+    for (int i = 0; i < kMaxRT; ++i)
+        if (i < nrt && rr + i * kRowsPass < rows) s[i] = tile[(rr + i * kRowsPass) * kTpr + c];
+
+    for (int t = 0; t < a.T; ++t) {
+        float d = a.dt[int64_t(b) * a.dt_sb + int64_t(t) * a.dt_st + h] + bias;
+        const int64_t bc = int64_t(b) * a.bc_sb + int64_t(t) * a.bc_st + int64_t(g) * a.bc_sg + 4 * c;
+        const float4 bq = load4(static_cast<const T *>(a.Bm) + bc);
+        const float4 cq = load4(static_cast<const T *>(a.Cm) + bc);
+        if (a.parent && t > 0) {
+            // start from the state after the parent token, when it is an earlier one
+            const int pt = a.parent[int64_t(b) * a.par_sb + t];
+            if (pt >= 0 && pt < t) {
+                const float *src = a.inter + ((int64_t(b) * a.T + pt) * a.H + h) * a.P * N;
+#pragma unroll
+                for (int i = 0; i < kMaxRT; ++i)
+                    if (i < nrt && rr + i * kRowsPass < rows)
+                        s[i] = *reinterpret_cast<const float4 *>(
+                            src + int64_t(r0 + rr + i * kRowsPass) * N + 4 * c);
             }
-            static_cast<T *>(a.out)[int64_t(b) * a.o_sb + int64_t(h) * a.o_sh + row] = from_f<T>(o);
+        }
+        if (a.softplus) d = d <= 20.f ? log1pf(expf(d)) : d;   // log(1 + e^d), = d to fp32 above 20
+        const float dA = expf(Ah * d);
+        __syncthreads();                            // x, z of token t staged
+        if (t + 1 < a.T) stage_xz(t + 1);           // the other buffer, read after the next sync
+        const float *xt = xs[t & 1], *zt = zs[t & 1];
+        T *orow = static_cast<T *>(a.out) + int64_t(b) * a.o_sb + int64_t(t) * a.o_st +
+                  int64_t(h) * a.o_sh + r0;
+        float *ir = a.inter ? a.inter + ((int64_t(b) * a.T + t) * a.H + h) * a.P * N : nullptr;
+#pragma unroll
+        for (int i = 0; i < kMaxRT; ++i) {
+            if (i >= nrt) break;
+            const int lr = rr + i * kRowsPass;        // local row
+            const bool live = lr < rows;              // false only when P < kRowsPass
+            float xv = 0.f, partial = 0.f;
+            if (live) {
+                xv = xt[lr];
+                const float u = d * xv;
+                s[i].x = fmaf(s[i].x, dA, u * bq.x);
+                s[i].y = fmaf(s[i].y, dA, u * bq.y);
+                s[i].z = fmaf(s[i].z, dA, u * bq.z);
+                s[i].w = fmaf(s[i].w, dA, u * bq.w);
+                if (ir) *reinterpret_cast<float4 *>(ir + int64_t(r0 + lr) * N + 4 * c) = s[i];
+                partial = fmaf(s[i].x, cq.x, fmaf(s[i].y, cq.y, fmaf(s[i].z, cq.z, s[i].w * cq.w)));
+            }
+            // sum over the row's kTpr lanes (contiguous within the warp)
+#pragma unroll
+            for (int off = kTpr / 2; off > 0; off >>= 1)
+                partial += __shfl_xor_sync(0xffffffffu, partial, off);
+            if (live && c == 0) {
+                float o = fmaf(Dh, xv, partial);
+                if (a.z) {
+                    const float zv = zt[lr];
+                    o *= zv / (1.f + expf(-zv));
+                }
+                orow[lr] = from_f<T>(o);
+            }
         }
     }
+    if (a.update) {
+#pragma unroll
+        for (int i = 0; i < kMaxRT; ++i)
+            if (i < nrt && rr + i * kRowsPass < rows)
+                __stcs(reinterpret_cast<float4 *>(st) + (rr + i * kRowsPass) * kTpr + c, s[i]);
+    }
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 152;
+    }
+    return n;
 }
 
 template <int N, typename T>
 cudaError_t launch_n(const SsuArgs &a, cudaStream_t s) {
-    constexpr int kRows = kSsuThreads / (N / 4);
-    const dim3 grid(unsigned((a.P + kRows * kR - 1) / (kRows * kR)), unsigned(a.H), unsigned(a.B));
-    k_ssu_step<N, T><<<grid, kSsuThreads, 0, s>>>(a);
+    constexpr int kRowsPass = kSsuThreads / (N / 4);
+    // the largest tile a thread's registers hold, halved while the grid is
+    // below two CTAs per SM (few sequences: spread the rows over more SMs)
+    int rows = a.P < kMaxRT * kRowsPass ? a.P : kMaxRT * kRowsPass;   // P / rows whole
+    const int64_t want = 2 * int64_t(sm_count());
+    while (rows / 2 >= kRowsPass && int64_t(a.B) * a.H * (a.P / rows) < want) rows /= 2;
+    unsigned int *err = nullptr;
+    cudaError_t e = device_error_word(&err);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(unsigned(a.P / rows), unsigned(a.H), unsigned(a.B));
+    k_ssu_tokens<N, T><<<grid, kSsuThreads, size_t(rows) * N * 4, s>>>(a, rows, err);
     return cudaGetLastError();
 }
 
@@ -137,7 +224,7 @@ cudaError_t launch_t(const SsuArgs &a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_ssu(const SsuArgs &a, cudaStream_t s) {
-    if (a.B == 0) return cudaSuccess;
+    if (a.B == 0 || a.T == 0) return cudaSuccess;
     return a.xdt == DT_BF16 ? launch_t<__nv_bfloat16>(a, s) : launch_t<float>(a, s);
 }
 

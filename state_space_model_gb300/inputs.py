@@ -113,22 +113,26 @@ def small_case(dtype="bf16", batch=2, seqlen=600, nheads=4, headdim=64,
 SSU_SHAPE = {"batch": 64, "nheads": 128, "headdim": 64, "dstate": 128, "ngroups": 8}
 
 
-def make_ssu_inputs(batch, nheads, headdim, dstate, ngroups, seed=20270, gated=True):
-    """Draw one decode step's inputs on the CPU: state [B,H,P,N] f32, x and z
+def make_ssu_inputs(batch, nheads, headdim, dstate, ngroups, seed=20270, gated=True,
+                    tokens=None):
+    """Draw decode-step inputs on the CPU: state [B,H,P,N] f32, x and z
     [B,H,P] bf16, raw dt [B,H] (softplus is applied by the step, after
-    dt_bias), dt_bias, A, D [H] f32, B and C [B,G,N] bf16 scaled by 1/sqrt(N)."""
+    dt_bias), dt_bias, A, D [H] f32, B and C [B,G,N] bf16 scaled by 1/sqrt(N).
+    With ``tokens`` = T the per-token tensors get a token axis after the batch
+    ([B,T,H,P], [B,T,H], [B,T,G,N])."""
     g = torch.Generator().manual_seed(seed)
     f32 = torch.float32
     Bn, H, P, N, G = batch, nheads, headdim, dstate, ngroups
+    tk = () if tokens is None else (tokens,)
     state = torch.randn((Bn, H, P, N), generator=g, dtype=f32) * 0.1
-    x = torch.randn((Bn, H, P), generator=g, dtype=f32)
-    Bm = torch.randn((Bn, G, N), generator=g, dtype=f32) * (1.0 / math.sqrt(N))
-    Cm = torch.randn((Bn, G, N), generator=g, dtype=f32) * (1.0 / math.sqrt(N))
-    dt_raw = torch.randn((Bn, H), generator=g, dtype=f32) * 0.5 - 2.0
+    x = torch.randn((Bn,) + tk + (H, P), generator=g, dtype=f32)
+    Bm = torch.randn((Bn,) + tk + (G, N), generator=g, dtype=f32) * (1.0 / math.sqrt(N))
+    Cm = torch.randn((Bn,) + tk + (G, N), generator=g, dtype=f32) * (1.0 / math.sqrt(N))
+    dt_raw = torch.randn((Bn,) + tk + (H,), generator=g, dtype=f32) * 0.5 - 2.0
     dt_bias = torch.randn((H,), generator=g, dtype=f32) * 0.1
     A = -torch.exp(torch.rand((H,), generator=g, dtype=f32) * math.log(16.0))
     D = torch.randn((H,), generator=g, dtype=f32)
-    z = torch.randn((Bn, H, P), generator=g, dtype=f32) if gated else None
+    z = torch.randn((Bn,) + tk + (H, P), generator=g, dtype=f32) if gated else None
     bf = torch.bfloat16
     return {"state": state, "x": x.to(bf), "dt": dt_raw, "dt_bias": dt_bias, "A": A,
             "B": Bm.to(bf), "C": Cm.to(bf), "D": D, "z": None if z is None else z.to(bf)}

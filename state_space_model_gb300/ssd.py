@@ -18,7 +18,8 @@ import torch
 from . import _native
 from ._native import SsdError, SsdTensor  # noqa: F401  (re-exported)
 
-_DTYPES = {torch.float32: _native.SSD_F32, torch.bfloat16: _native.SSD_BF16}
+_DTYPES = {torch.float32: _native.SSD_F32, torch.bfloat16: _native.SSD_BF16,
+           torch.int32: _native.SSD_I32}
 
 
 def _desc(t: torch.Tensor | None):
@@ -136,6 +137,29 @@ def state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplu
                                        1 if dt_softplus else 0, ngroups, _desc(out),
                                        _stream(dev)),
                   "ssd_state_update")
+    return out
+
+
+def state_update_tokens(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
+                        ngroups=1, *, intermediate_states=None, parent=None, update_state=True,
+                        out=None):
+    """T decode tokens per sequence (``ssd_state_update_tokens``): x, z, out
+    [B,T,H,P]; dt [B,T,H]; B, C [B,T,G,N]; optional intermediate_states
+    [B,T,H,P,N] f32 (the state after every token) and parent [B,T] int32
+    (token t starts from the state after token parent[b,t] when that is an
+    earlier token).  Updates ``state`` in place unless ``update_state`` is
+    false; returns ``out``."""
+    dev = _device_of(state, x, dt, A, B, C, D, z, dt_bias, intermediate_states, parent, out)
+    if out is None:
+        out = torch.empty(x.shape, dtype=x.dtype, device=dev)
+    lib = _native.load()
+    _native.check(lib.ssd_state_update_tokens(_desc(state), _desc(x), _desc(dt), _desc(A),
+                                              _desc(B), _desc(C), _desc(D), _desc(z),
+                                              _desc(dt_bias), 1 if dt_softplus else 0, ngroups,
+                                              _desc(out), _desc(intermediate_states),
+                                              _desc(parent), 1 if update_state else 0,
+                                              _stream(dev)),
+                  "ssd_state_update_tokens")
     return out
 
 

@@ -294,3 +294,47 @@ def test_state_update_error_paths(lib):
     assert call(state=e0, x=tens((0, H, P), BF16, ptr=x.data), dt=tens((0, H), F32, ptr=dt.data),
                 Bm=tens((0, G, N), BF16, ptr=Bm.data), Cm=tens((0, G, N), BF16, ptr=Cm.data),
                 out=tens((0, H, P), BF16, ptr=out.data)) == 0
+
+
+def test_state_update_tokens_error_paths(lib):
+    """ssd_state_update_tokens' host checks (fake pointers, never dereferenced)."""
+    p = ctypes.pointer
+    I32 = 2
+    Bn, T, H, P, N, G = 2, 3, 4, 64, 128, 2
+    base = FAKE + (1 << 34)
+    state = tens((Bn, H, P, N), F32, ptr=base)
+    x = tens((Bn, T, H, P), BF16, ptr=base + (1 << 24))
+    dt = tens((Bn, T, H), F32, ptr=base + (2 << 24))
+    A = tens((H,), F32, ptr=base + (3 << 24))
+    Bm = tens((Bn, T, G, N), BF16, ptr=base + (4 << 24))
+    Cm = tens((Bn, T, G, N), BF16, ptr=base + (5 << 24))
+    out = tens((Bn, T, H, P), BF16, ptr=base + (6 << 24))
+    inter = tens((Bn, T, H, P, N), F32, ptr=base + (8 << 24))
+    parent = tens((Bn, T), I32, ptr=base + (7 << 24))
+
+    def call(**kw):
+        a = dict(state=state, x=x, dt=dt, A=A, Bm=Bm, Cm=Cm, out=out, inter=inter, parent=parent,
+                 upd=1)
+        a.update(kw)
+        q = lambda t: None if t is None else p(t)
+        return lib.ssd_state_update_tokens(q(a["state"]), q(a["x"]), q(a["dt"]), q(a["A"]),
+                                           q(a["Bm"]), q(a["Cm"]), None, None, None, 0, G,
+                                           q(a["out"]), q(a["inter"]), q(a["parent"]), a["upd"],
+                                           None)
+
+    assert call(inter=None) == 1 and "parent needs intermediate_states" in detail(lib)
+    assert call(parent=tens((Bn, T), F32, ptr=parent.data)) == 1 and "dtype" in detail(lib)
+    assert call(x=tens((Bn, H, P), BF16, ptr=x.data)) == 1 and "ndim" in detail(lib)
+    assert call(dt=tens((Bn, T + 1, H), F32, ptr=dt.data)) == 1 and "shape" in detail(lib)
+    assert call(inter=tens((Bn, T, H, P, N), BF16, ptr=inter.data)) == 1
+    assert call(inter=tens((Bn, T + 1, H, P, N), F32, ptr=inter.data)) == 1
+    assert call(inter=tens((Bn, T, H, P, N), F32, ptr=inter.data + 4)) == 3
+    assert call(inter=tens((Bn, T, H, P, N), F32, ptr=base)) == 1 and "overlaps" in detail(lib)
+    # int32 is accepted only where it is asked for
+    assert call(x=tens((Bn, T, H, P), I32, ptr=x.data)) == 1 and "dtype" in detail(lib)
+    # no parent and no cache is valid as far as the host checks go; T = 0 launches nothing
+    e = lambda shape, dtype, t: tens(shape, dtype, ptr=t.data)
+    assert call(x=e((Bn, 0, H, P), BF16, x), dt=e((Bn, 0, H), F32, dt),
+                Bm=e((Bn, 0, G, N), BF16, Bm), Cm=e((Bn, 0, G, N), BF16, Cm),
+                out=e((Bn, 0, H, P), BF16, out), inter=e((Bn, 0, H, P, N), F32, inter),
+                parent=e((Bn, 0), I32, parent)) == 0

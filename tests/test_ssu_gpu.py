@@ -113,3 +113,98 @@ def test_state_update_is_deterministic(ssd):
         runs.append((o.clone(), st))
     torch.cuda.synchronize()
     assert torch.equal(runs[0][0], runs[1][0]) and torch.equal(runs[0][1], runs[1][1])
+
+
+# ---- several tokens per call -------------------------------------------------
+
+def make_tokens(B, T, H, P, N, G, dtype, seed, z=True, bias=True, softplus=True):
+    g = torch.Generator().manual_seed(seed)
+    r = lambda *s: torch.randn(s, generator=g)
+    dt_raw = r(B, T, H) * 0.5 - 2.0
+    return dict(
+        state=0.5 * r(B, H, P, N),
+        x=r(B, T, H, P).to(dtype),
+        dt=dt_raw if softplus else torch.nn.functional.softplus(dt_raw),
+        A=-torch.exp(torch.rand(H, generator=g) * math.log(16.0)),
+        Bm=(r(B, T, G, N) / math.sqrt(N)).to(dtype),
+        Cm=(r(B, T, G, N) / math.sqrt(N)).to(dtype),
+        D=r(H),
+        z=r(B, T, H, P).to(dtype) if z else None,
+        dt_bias=0.3 * r(H) if bias else None,
+        dt_softplus=softplus,
+        ngroups=G,
+    )
+
+
+def random_tree(B, T, seed):
+    """parent[b, t] in [-1, t): a random draft tree per sequence (-1 = previous token)."""
+    g = torch.Generator().manual_seed(seed)
+    par = torch.full((B, T), -1, dtype=torch.int32)
+    for t in range(1, T):
+        par[:, t] = torch.randint(-1, t, (B,), generator=g, dtype=torch.int32)
+    return par
+
+
+TOKEN_CASES = [
+    # (B, T, H, P, N, G, dtype, cache, tree, update)
+    (4, 4, 16, 64, 128, 2, torch.bfloat16, True, True, True),
+    (3, 6, 8, 64, 128, 8, torch.bfloat16, True, False, False),
+    (2, 3, 6, 32, 64, 3, torch.float32, False, False, True),
+    (64, 2, 32, 64, 128, 8, torch.bfloat16, False, False, True),    # a full grid: whole heads
+    (1, 5, 4, 128, 128, 1, torch.float32, True, True, True),        # few heads: rows split
+    (2, 3, 4, 16, 16, 2, torch.bfloat16, True, True, False),        # P below a pass of rows
+    (5, 1, 3, 128, 32, 1, torch.float32, True, False, True),
+]
+
+
+@pytest.mark.parametrize("case", TOKEN_CASES, ids=lambda c: f"B{c[0]}T{c[1]}H{c[2]}P{c[3]}N{c[4]}"
+                         f"G{c[5]}-{str(c[6])[6:]}-cache{int(c[7])}tree{int(c[8])}up{int(c[9])}")
+def test_state_update_tokens_matches_oracle(ssd, case):
+    B, T, H, P, N, G, dtype, cache, tree, update = case
+    inp = make_tokens(B, T, H, P, N, G, dtype, seed=B * 100 + T * 10 + N)
+    parent = random_tree(B, T, seed=T) if tree else None
+    out_ref, fin_ref, cache_ref = orc.ssu_tokens(**inp, parent=parent, update_state=update)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    state = dev.pop("state").clone()
+    inter = torch.empty((B, T, H, P, N), dtype=torch.float32, device="cuda") if cache else None
+    out = ssd.state_update_tokens(state, dev["x"], dev["dt"], dev["A"], dev["Bm"], dev["Cm"],
+                                  D=dev["D"], z=dev["z"], dt_bias=dev["dt_bias"],
+                                  dt_softplus=dev["dt_softplus"], ngroups=G,
+                                  intermediate_states=inter,
+                                  parent=None if parent is None else parent.cuda(),
+                                  update_state=update)
+    torch.cuda.synchronize()
+    assert out.dtype == dtype and out.shape == (B, T, H, P)
+    bar = 2e-2 if dtype == torch.bfloat16 else 1e-4
+    assert rel(out.double().cpu().numpy(), out_ref) <= bar
+    if update:
+        assert rel(state.double().cpu().numpy(), fin_ref) <= 1e-4
+    else:   # untouched, bit for bit
+        assert torch.equal(state.cpu(), inp["state"])
+    if cache:
+        assert rel(inter.double().cpu().numpy(), cache_ref) <= 1e-4
+
+
+def test_one_token_call_equals_the_single_step(ssd):
+    inp = make_step(6, 24, 64, 128, 4, torch.bfloat16, seed=21, z=True, bias=True, softplus=True)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    st1, st2 = dev["state"].clone(), dev["state"].clone()
+    o1 = ssd.state_update(st1, dev["x"], dev["dt"], dev["A"], dev["Bm"], dev["Cm"], D=dev["D"],
+                          z=dev["z"], dt_bias=dev["dt_bias"], dt_softplus=True, ngroups=4)
+    u = lambda t: None if t is None else t.unsqueeze(1)
+    o2 = ssd.state_update_tokens(st2, u(dev["x"]), u(dev["dt"]), dev["A"], u(dev["Bm"]),
+                                 u(dev["Cm"]), D=dev["D"], z=u(dev["z"]), dt_bias=dev["dt_bias"],
+                                 dt_softplus=True, ngroups=4)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2[:, 0]) and torch.equal(st1, st2)
+
+
+def test_state_update_tokens_zero_tokens_is_a_no_op(ssd):
+    inp = make_tokens(2, 0, 4, 64, 128, 2, torch.bfloat16, seed=1)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    state = dev["state"].clone()
+    out = ssd.state_update_tokens(state, dev["x"], dev["dt"], dev["A"], dev["Bm"], dev["Cm"],
+                                  D=dev["D"], z=dev["z"], dt_bias=dev["dt_bias"],
+                                  dt_softplus=True, ngroups=2)
+    torch.cuda.synchronize()
+    assert out.shape == (2, 0, 4, 64) and torch.equal(state, dev["state"])
