@@ -157,13 +157,22 @@ class ClockSampler:
 # traffic from a committed ncu summary, valid only for the kernel source it was taken on
 
 
+# the sources each recorded kernel is built from (a change elsewhere leaves
+# its DRAM traffic record valid)
+KERNEL_SOURCES = {
+    "ssd_fused": ["ssd_fused.cu", "ptx_sm100.cuh", "ssd_tc.cuh", "ssd_internal.h"],
+    "k_ssu_tokens": ["ssd_ssu.cu", "ptx_sm100.cuh", "ssd_internal.h"],
+}
+
+
 def kernel_source_hash(stage: str) -> str:
     csrc = os.path.join(ROOT, "state_space_model_gb300", "csrc")
+    names = KERNEL_SOURCES.get(stage) or sorted(
+        n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh", ".h")))
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -357,6 +366,9 @@ def run_ssu(args, world, rank, local):
     clk = clocks.stop()
     pk = peaks()
     nbytes = ssu_bytes(Bn, H, P, N, G, T, cached=T > 1)
+    wname = "ssu_decode" if T == 1 else f"ssu_decode_{T}_tokens"
+    if Bn != gen.SSU_SHAPE["batch"]:
+        wname += f"_b{Bn}"
     achieved = nbytes / (ms / 1e3) / 1e9
     if rank == 0:
         line = {
@@ -364,7 +376,7 @@ def run_ssu(args, world, rank, local):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded; see state_space_model_gb300/inputs.py)",
-            "config": {"workload": "ssu_decode" if T == 1 else f"ssu_decode_{T}_tokens",
+            "config": {"workload": wname,
                        "batch": Bn, "tokens": T, "nheads": H, "headdim": P,
                        "dstate": N, "ngroups": G, "gated": True, "dt_softplus": True,
                        "state_cache": T > 1,
@@ -372,7 +384,8 @@ def run_ssu(args, world, rank, local):
                        if Bn * H * P * N * 4 > L2_BYTES else "state smaller than L2"},
             "roofline": {"bound": "hbm", "kernel": "k_ssu_tokens", "achieved": achieved,
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-                         "traffic": None, "algorithmic_bytes": nbytes, "kernel_ms": ms,
+                         "traffic": recorded_traffic("k_ssu_tokens", wname),
+                         "algorithmic_bytes": nbytes, "kernel_ms": ms,
                          "peak_source": pk["source"]},
             "gpu_launches": args.steps, "launch": "CUDA graph replay, one kernel per step",
             "clocks": clk,
