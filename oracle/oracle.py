@@ -361,3 +361,72 @@ def ssu_tokens(state, x, dt, A, Bm, Cm, D=None, z=None, dt_bias=None, dt_softplu
         if update_state and T > 0:
             final[b] = run[0].numpy()
     return out, final, cache
+
+
+def causal_conv1d(xBC, weight, bias=None, conv_state=None, silu=True):
+    """Causal depthwise convolution over the token axis, then SiLU -- the
+    convolution that prepares x, B and C in the Mamba-2 mixer ("Optimizing
+    Nemotron v3 Super in TensorRT-LLM", sections 8 "CausalConv1d Optimization"
+    and 10.5), in float64.
+
+    xBC [B, L, Dc]; weight [Dc, W]; bias [Dc] or None; conv_state [B, Dc, W]
+    or None: the last W inputs before this call, oldest first (zeros when
+    None).  With u the inputs preceded by that state,
+
+        out[b, t, c] = silu(bias[c] + sum_k weight[c, k] u[b, t - (W - 1) + k, c])
+
+    so weight[:, W - 1] multiplies the current token.  Returns
+    ``(out [B, L, Dc], new_state [B, Dc, W], windows [B, L, Dc, W])``:
+    new_state holds the last W inputs of the concatenation, windows[:, t] the
+    last W inputs up to and including token t (the state after token t).
+    """
+    xv = _as_cpu(xBC).to(torch.float64).numpy()
+    w = _as_cpu(weight).to(torch.float64).numpy()
+    Bn, L, Dc = xv.shape
+    W = w.shape[1]
+    if w.shape[0] != Dc:
+        raise ValueError("oracle: weight must be [Dc, W]")
+    bv = np.zeros(Dc) if bias is None else _as_cpu(bias).to(torch.float64).numpy()
+    st = (np.zeros((Bn, Dc, W)) if conv_state is None
+          else _as_cpu(conv_state).to(torch.float64).numpy())
+    u = np.concatenate([st.transpose(0, 2, 1), xv], axis=1)      # [B, W + L, Dc]
+    out = np.empty((Bn, L, Dc))
+    windows = np.empty((Bn, L, Dc, W))
+    for t in range(L):
+        win = u[:, t + 1:t + 1 + W, :]                            # inputs t-W+1 .. t
+        pre = bv[None, :] + np.einsum("bkc,ck->bc", win, w)
+        out[:, t] = pre / (1.0 + np.exp(-pre)) if silu else pre
+        windows[:, t] = win.transpose(0, 2, 1)
+    new_state = u[:, L:L + W, :].transpose(0, 2, 1).copy()
+    return out, new_state, windows
+
+
+def dt_prologue(dt, dt_bias=None, dt_softplus=True):
+    """dt' = dt + dt_bias, then softplus(dt') = log(1 + exp(dt')) when asked
+    (the dt preparation of the SSU reference, "Optimizing Nemotron v3 Super in
+    TensorRT-LLM", section 6.2), in float64.  dt [..., H], dt_bias [H]."""
+    d = _as_cpu(dt).to(torch.float64).numpy()
+    if dt_bias is not None:
+        d = d + _as_cpu(dt_bias).to(torch.float64).numpy()
+    return np.logaddexp(0.0, d) if dt_softplus else d
+
+
+def split_xbc(xbc, nheads, headdim, ngroups, dstate):
+    """The channel order of the mixer's convolution output: x (H P channels),
+    then B (G N), then C (G N).  [B, L, Dc] -> x [B, L, H, P], B and C
+    [B, L, G, N] (numpy views)."""
+    Bn, L, Dc = xbc.shape
+    hp, gn = nheads * headdim, ngroups * dstate
+    if Dc != hp + 2 * gn:
+        raise ValueError("oracle: Dc must be H P + 2 G N")
+    return (xbc[..., :hp].reshape(Bn, L, nheads, headdim),
+            xbc[..., hp:hp + gn].reshape(Bn, L, ngroups, dstate),
+            xbc[..., hp + gn:].reshape(Bn, L, ngroups, dstate))
+
+
+def gate(y, z):
+    """y silu(z) = y z / (1 + exp(-z)), the output gate of the mixer, in float64."""
+    yv = np.asarray(y, dtype=np.float64) if not isinstance(y, torch.Tensor) else \
+        _as_cpu(y).to(torch.float64).numpy()
+    zv = _as_cpu(z).to(torch.float64).numpy()
+    return yv * (zv / (1.0 + np.exp(-zv)))
