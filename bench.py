@@ -393,14 +393,96 @@ def run_ssu(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+PROLOGUE_METRIC = ("mixer prologue (conv1d + SiLU + x/B/C split + dt softplus) tokens/s at "
+                   "Mamba-2 2.7B layer shape; % of HBM roofline")
+
+
+def prologue_bytes(Bn, L, H, P, G, N, W, es=2):
+    """Compulsory HBM bytes of one prologue call: xBC read and x, B, C written
+    (es bytes each), raw dt read and dt' written (f32), the conv state read and
+    written, the conv weights and biases, dt_bias."""
+    Dc = H * P + 2 * G * N
+    return 2 * Bn * L * Dc * es + 2 * Bn * L * H * 4 + 2 * Bn * Dc * W * es + Dc * (W + 1) * 4 \
+        + H * 4
+
+
+def run_prologue(args, world, rank, local):
+    """One ssd_mixer_prologue call per timed iteration on the Mamba-2 2.7B mixer
+    shape (d_inner 5120 = 80 heads x 64, one group of 128 states, width-4
+    convolution), conv state carried in place."""
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the CUDA path has no CPU fallback)")
+    from state_space_model_gb300 import build, ssd
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    w = gen.WORKLOADS[args.workload]
+    Bn = args.batch if args.batch is not None else w.batch
+    L, H, P, G, N, W = w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, 4
+    cpu = gen.make_prologue_inputs(Bn, L, H, P, G, N, W, seed=20280 + rank)
+    d = {k: v.to(dev) for k, v in cpu.items()}
+    outs = (torch.empty((Bn, L, H, P), dtype=torch.bfloat16, device=dev),
+            torch.empty((Bn, L, G, N), dtype=torch.bfloat16, device=dev),
+            torch.empty((Bn, L, G, N), dtype=torch.bfloat16, device=dev),
+            torch.empty((Bn, L, H), dtype=torch.float32, device=dev))
+
+    def step():
+        ssd.mixer_prologue(d["xBC"], d["conv_weight"], d["dt"], H, P, G, N,
+                           conv_bias=d["conv_bias"], conv_state=d["conv_state"],
+                           dt_bias=d["dt_bias"], dt_softplus=True, out=outs)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark_on()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_off()
+    barrier(world)
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
+    clk = clocks.stop()
+    pk = peaks()
+    nbytes = prologue_bytes(Bn, L, H, P, G, N, W)
+    achieved = nbytes / (ms / 1e3) / 1e9
+    in_bytes = Bn * L * (H * P + 2 * G * N) * 2
+    if rank == 0:
+        line = {
+            "metric": PROLOGUE_METRIC, "value": world * Bn * L / (ms / 1e3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; see state_space_model_gb300/inputs.py)",
+            "config": {"workload": f"prologue_{w.name}", "batch": Bn, "seqlen": L, "nheads": H,
+                       "headdim": P, "ngroups": G, "dstate": N, "conv_width": W,
+                       "conv_state": True, "dt_softplus": True,
+                       "l2": f"xBC {in_bytes / 1e6:.0f} MB, larger than L2"
+                       if in_bytes > L2_BYTES else "xBC smaller than L2"},
+            "roofline": {"bound": "hbm", "kernel": "k_conv_prologue", "achieved": achieved,
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                         "traffic": None, "algorithmic_bytes": nbytes, "kernel_ms": ms,
+                         "peak_source": pk["source"]},
+            "gpu_launches": 2 * args.steps, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["prefill", "ssu"], default="prefill",
-                    help="prefill: ssd_chunked_fwd (the headline); ssu: one decode step")
+    ap.add_argument("--op", choices=["prefill", "ssu", "prologue"], default="prefill",
+                    help="prefill: ssd_chunked_fwd (the headline); ssu: one decode step; "
+                         "prologue: ssd_mixer_prologue on the workload's mixer shape")
     ap.add_argument("--workload", default=gen.HEADLINE, choices=sorted(gen.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -421,8 +503,8 @@ def main():
     if args.impl == "reference":
         run_reference(args, w, world, rank)
         return
-    if args.op == "ssu":
-        run_ssu(args, world, rank, local)
+    if args.op in ("ssu", "prologue"):
+        (run_ssu if args.op == "ssu" else run_prologue)(args, world, rank, local)
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()

@@ -236,6 +236,45 @@ ssd_status ssd_state_update_tokens(ssd_tensor *state, const ssd_tensor *x, const
                                    ssd_tensor *intermediate_states, const ssd_tensor *parent,
                                    int32_t update_state, void *stream);
 
+/* ---- mixer prologue ----------------------------------------------------------
+ * The steps of the Mamba-2 mixer between its input projection and the scan, in
+ * one pass: the causal depthwise convolution with SiLU over the xBC channels,
+ * the split of its output into x, B and C, and the dt preparation -- "Optimizing
+ * Nemotron v3 Super in TensorRT-LLM", sections 6.2 (dt + dt_bias, softplus),
+ * 7.1 (the split written directly in the layout the scan reads), 8
+ * ("CausalConv1d Optimization") and 10.3 / 10.5 (the conv state and its
+ * per-token windows).  With u the inputs of a sequence preceded by conv_state
+ * (its last W inputs so far, oldest first; zeros when conv_state is NULL):
+ *
+ *   xbc[b, t, c] = silu(conv_bias[c] + sum_k conv_weight[c, k] u[b, t - (W-1) + k, c])
+ *   x = xbc[..., 0 : H P] as [B, L, H, P]
+ *   B = xbc[..., H P : H P + G N] as [B, L, G, N],   C = xbc[..., H P + G N :]
+ *   dt_out = dt + dt_bias, then log(1 + exp(.)) if dt_softplus (kept as is above
+ *            20, the same in fp32)
+ *   conv_state <- the last W inputs of u (in place);
+ *   conv_windows[b, t] = the last W inputs up to and including token t
+ *
+ * Shapes, dtypes and layouts:
+ *   xBC [B, L, Dc] bf16 or f32, Dc = H P + 2 G N (H and P from x, N from B)
+ *   conv_weight [Dc, W] f32, packed, W in 1..4 (weight[:, W-1] takes the
+ *     current token); conv_bias [Dc] f32, optional
+ *   conv_state [B, Dc, W] dtype of xBC, packed, optional
+ *   conv_windows [B, L, Dc, W] dtype of xBC, packed, optional
+ *   dt, dt_out [B, L, H] f32; dt_bias [H] f32, optional
+ *   x [B, L, H, P], B and C [B, L, G, N], dtype of xBC (outputs)
+ * The outputs are what ssd_chunked_fwd takes as x, dt, B and C.  Alignment:
+ * xBC, x, B, C base pointers 16-byte aligned and their outer strides multiples
+ * of 16 bytes.  Aliasing: no output (the conv state included) may overlap an
+ * input or another output.  P and N in {16, 32, 64, 128}.  Errors,
+ * ownership and streams as above; one launch (two when conv_state is given and
+ * a sequence is split over several CTAs, which needs L > 8), no workspace. */
+ssd_status ssd_mixer_prologue(const ssd_tensor *xBC, const ssd_tensor *conv_weight,
+                              const ssd_tensor *conv_bias, ssd_tensor *conv_state,
+                              ssd_tensor *conv_windows, const ssd_tensor *dt,
+                              const ssd_tensor *dt_bias, int32_t dt_softplus, int64_t ngroups,
+                              ssd_tensor *x, ssd_tensor *B, ssd_tensor *C, ssd_tensor *dt_out,
+                              void *stream);
+
 /* ---- stage entry points (the four steps of ssd_chunked_fwd, one call each;
  *      same conventions; used to check each step on its own) ---------------- */
 

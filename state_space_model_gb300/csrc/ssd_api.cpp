@@ -592,6 +592,123 @@ ssd_status ssd_state_update_tokens(ssd_tensor *state, const ssd_tensor *x, const
                              out, intermediate_states, parent, update_state, stream);
 }
 
+ssd_status ssd_mixer_prologue(const ssd_tensor *xBC, const ssd_tensor *conv_weight,
+                              const ssd_tensor *conv_bias, ssd_tensor *conv_state,
+                              ssd_tensor *conv_windows, const ssd_tensor *dt,
+                              const ssd_tensor *dt_bias, int32_t dt_softplus, int64_t ngroups,
+                              ssd_tensor *x, ssd_tensor *Bm, ssd_tensor *Cm, ssd_tensor *dt_out,
+                              void *stream) {
+    if (!xBC || !x || !Bm || !conv_weight)
+        return fail(SSD_ERR_INVALID_ARG, "xBC / conv_weight / x / B: null tensor descriptor");
+    if (xBC->ndim != 3) return fail(SSD_ERR_INVALID_ARG, "xBC: ndim %d, expected 3", xBC->ndim);
+    if (x->ndim != 4 || Bm->ndim != 4)
+        return fail(SSD_ERR_INVALID_ARG, "x / B: ndim must be 4");
+    if (conv_weight->ndim != 2)
+        return fail(SSD_ERR_INVALID_ARG, "conv_weight: ndim %d, expected 2", conv_weight->ndim);
+    const int64_t Bn = xBC->shape[0], L = xBC->shape[1], Dc = xBC->shape[2];
+    const int64_t H = x->shape[2], P = x->shape[3], N = Bm->shape[3], G = ngroups,
+                  W = conv_weight->shape[1];
+    if (Bn < 0 || L < 0) return fail(SSD_ERR_INVALID_ARG, "negative batch or seqlen");
+    if (H <= 0 || G <= 0)
+        return fail(SSD_ERR_INVALID_ARG, "nheads %lld / ngroups %lld must be positive",
+                    (long long)H, (long long)G);
+    if (!supported_dim(P) || !supported_dim(N))
+        return fail(SSD_ERR_UNSUPPORTED, "headdim %lld / dstate %lld unsupported (16, 32, 64 or "
+                    "128)", (long long)P, (long long)N);
+    if (Dc != H * P + 2 * G * N)
+        return fail(SSD_ERR_INVALID_ARG, "xBC has %lld channels; nheads * headdim + 2 * ngroups * "
+                    "dstate = %lld", (long long)Dc, (long long)(H * P + 2 * G * N));
+    if (W < 1 || W > 4)
+        return fail(SSD_ERR_UNSUPPORTED, "conv width %lld unsupported (1 to 4)", (long long)W);
+    if (Bn > 65535 || (L + 63) / 64 > 65535)
+        return fail(SSD_ERR_UNSUPPORTED, "batch %lld above 65535 or seqlen %lld above 4194240",
+                    (long long)Bn, (long long)L);
+    const int xdt = xBC->dtype;
+    const int64_t sin[3] = {Bn, L, Dc}, sw[2] = {Dc, W}, sb[1] = {Dc}, sst[3] = {Bn, Dc, W},
+                  swin[4] = {Bn, L, Dc, W}, sdt[3] = {Bn, L, H}, sh[1] = {H},
+                  sx[4] = {Bn, L, H, P}, sbc[4] = {Bn, L, G, N};
+    ssd_status st;
+    if ((st = check_tensor(xBC, "xBC", 3, sin, -1, false, true))) return st;
+    if ((st = check_tensor(conv_weight, "conv_weight", 2, sw, SSD_F32, true, false))) return st;
+    if (conv_bias && (st = check_tensor(conv_bias, "conv_bias", 1, sb, SSD_F32, true, false)))
+        return st;
+    if (conv_state && (st = check_tensor(conv_state, "conv_state", 3, sst, xdt, true, false)))
+        return st;
+    if (conv_windows &&
+        (st = check_tensor(conv_windows, "conv_windows", 4, swin, xdt, true, false)))
+        return st;
+    if ((st = check_tensor(dt, "dt", 3, sdt, SSD_F32, false, false))) return st;
+    if (dt_bias && (st = check_tensor(dt_bias, "dt_bias", 1, sh, SSD_F32, true, false))) return st;
+    if ((st = check_tensor(x, "x", 4, sx, xdt, false, true))) return st;
+    if ((st = check_tensor(Bm, "B", 4, sbc, xdt, false, true))) return st;
+    if ((st = check_tensor(Cm, "C", 4, sbc, xdt, false, true))) return st;
+    if ((st = check_tensor(dt_out, "dt_out", 3, sdt, SSD_F32, false, false))) return st;
+
+    // every output against every input and each other; the conv state is
+    // updated in place, so it may overlap nothing else
+    const Range ins[] = {range_of(xBC), range_of(conv_weight), range_of(conv_bias),
+                         range_of(dt), range_of(dt_bias)};
+    const char *in_names[] = {"xBC", "conv_weight", "conv_bias", "dt", "dt_bias"};
+    const Range outs[] = {range_of(x), range_of(Bm), range_of(Cm), range_of(dt_out),
+                          range_of(conv_state), range_of(conv_windows)};
+    const char *out_names[] = {"x", "B", "C", "dt_out", "conv_state", "conv_windows"};
+    for (int o = 0; o < 6; ++o) {
+        for (int i = 0; i < 5; ++i)
+            if (overlap(outs[o], ins[i]))
+                return fail(SSD_ERR_INVALID_ARG, "%s overlaps %s", out_names[o], in_names[i]);
+        for (int o2 = o + 1; o2 < 6; ++o2)
+            if (overlap(outs[o], outs[o2]))
+                return fail(SSD_ERR_INVALID_ARG, "%s overlaps %s", out_names[o], out_names[o2]);
+    }
+    if (Bn == 0 || L == 0) return ok();
+    auto dp = [](const ssd_tensor *t) -> const void * { return t ? t->data : nullptr; };
+    if ((st = check_device_ptrs({{dp(xBC), "xBC"}, {dp(conv_weight), "conv_weight"},
+                                 {dp(conv_bias), "conv_bias"}, {dp(conv_state), "conv_state"},
+                                 {dp(conv_windows), "conv_windows"}, {dp(dt), "dt"},
+                                 {dp(dt_bias), "dt_bias"}, {dp(x), "x"}, {dp(Bm), "B"},
+                                 {dp(Cm), "C"}, {dp(dt_out), "dt_out"}})))
+        return st;
+    ssd::MixerArgs a;
+    a.B = int(Bn);
+    a.L = L;
+    a.H = int(H);
+    a.P = int(P);
+    a.G = int(G);
+    a.N = int(N);
+    a.Dc = int(Dc);
+    a.W = int(W);
+    a.xdt = xdt;
+    a.softplus = dt_softplus ? 1 : 0;
+    a.xBC = xBC->data;
+    a.in_sb = xBC->stride[0];
+    a.in_sl = xBC->stride[1];
+    a.conv_w = static_cast<const float *>(conv_weight->data);
+    a.conv_b = conv_bias ? static_cast<const float *>(conv_bias->data) : nullptr;
+    a.state = conv_state ? conv_state->data : nullptr;
+    a.windows = conv_windows ? conv_windows->data : nullptr;
+    a.dt = static_cast<const float *>(dt->data);
+    a.dt_sb = dt->stride[0];
+    a.dt_sl = dt->stride[1];
+    a.dt_bias = dt_bias ? static_cast<const float *>(dt_bias->data) : nullptr;
+    a.dt_out = static_cast<float *>(dt_out->data);
+    a.do_sb = dt_out->stride[0];
+    a.do_sl = dt_out->stride[1];
+    a.x = x->data;
+    a.x_sb = x->stride[0];
+    a.x_sl = x->stride[1];
+    a.x_sh = x->stride[2];
+    a.Bo = Bm->data;
+    a.b_sb = Bm->stride[0];
+    a.b_sl = Bm->stride[1];
+    a.b_sg = Bm->stride[2];
+    a.Co = Cm->data;
+    a.c_sb = Cm->stride[0];
+    a.c_sl = Cm->stride[1];
+    a.c_sg = Cm->stride[2];
+    return cuda_status(ssd::launch_mixer_prologue(a, static_cast<cudaStream_t>(stream)),
+                       "mixer prologue");
+}
+
 ssd_status ssd_stage_chunk_cumsum(const ssd_tensor *dt, const ssd_tensor *A, int64_t chunk_size,
                                   ssd_tensor *G, void *stream) {
     if (!dt) return fail(SSD_ERR_INVALID_ARG, "dt: null tensor descriptor");

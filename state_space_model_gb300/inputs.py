@@ -136,3 +136,21 @@ def make_ssu_inputs(batch, nheads, headdim, dstate, ngroups, seed=20270, gated=T
     bf = torch.bfloat16
     return {"state": state, "x": x.to(bf), "dt": dt_raw, "dt_bias": dt_bias, "A": A,
             "B": Bm.to(bf), "C": Cm.to(bf), "D": D, "z": None if z is None else z.to(bf)}
+
+
+def make_prologue_inputs(batch, seqlen, nheads, headdim, ngroups, dstate, width=4, seed=20280):
+    """Draw the mixer prologue's inputs on the CPU: xBC [B, L, H P + 2 G N]
+    ~ N(0, 1) bf16, conv weight [Dc, W] ~ N(0, 1/W) and bias [Dc] ~ N(0, 0.1^2)
+    f32, conv state [B, Dc, W] ~ N(0, 1) bf16, raw dt [B, L, H] ~ N(-2, 0.5)
+    and dt_bias [H] ~ N(0, 0.1^2) f32."""
+    g = torch.Generator().manual_seed(seed)
+    f32, bf = torch.float32, torch.bfloat16
+    Dc = nheads * headdim + 2 * ngroups * dstate
+    xBC = torch.randn((batch, seqlen, Dc), generator=g, dtype=f32).to(bf)
+    w = torch.randn((Dc, width), generator=g, dtype=f32) / math.sqrt(width)
+    b = torch.randn((Dc,), generator=g, dtype=f32) * 0.1
+    st = torch.randn((batch, Dc, width), generator=g, dtype=f32).to(bf)
+    dt = torch.randn((batch, seqlen, nheads), generator=g, dtype=f32) * 0.5 - 2.0
+    dt_bias = torch.randn((nheads,), generator=g, dtype=f32) * 0.1
+    return {"xBC": xBC, "conv_weight": w, "conv_bias": b, "conv_state": st, "dt": dt,
+            "dt_bias": dt_bias}

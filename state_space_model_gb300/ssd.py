@@ -163,6 +163,33 @@ def state_update_tokens(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_
     return out
 
 
+def mixer_prologue(xBC, conv_weight, dt, nheads, headdim, ngroups, dstate, *, conv_bias=None,
+                   conv_state=None, conv_windows=None, dt_bias=None, dt_softplus=True,
+                   out=None):
+    """Causal conv1d + SiLU over xBC [B,L,Dc], split into x [B,L,H,P], B and C
+    [B,L,G,N], and dt' = softplus(dt + dt_bias) [B,L,H] f32
+    (``ssd_mixer_prologue``).  ``conv_state`` [B,Dc,W] is read as the left
+    context and updated in place; ``conv_windows`` [B,L,Dc,W] receives the
+    window after every token.  Returns ``(x, B, C, dt')``; ``out`` may give
+    those four buffers."""
+    dev = _device_of(xBC, conv_weight, dt, conv_bias, conv_state, conv_windows, dt_bias)
+    Bn, L, _ = xBC.shape
+    if out is None:
+        out = (torch.empty((Bn, L, nheads, headdim), dtype=xBC.dtype, device=dev),
+               torch.empty((Bn, L, ngroups, dstate), dtype=xBC.dtype, device=dev),
+               torch.empty((Bn, L, ngroups, dstate), dtype=xBC.dtype, device=dev),
+               torch.empty((Bn, L, nheads), dtype=torch.float32, device=dev))
+    x, Bm, Cm, dt_out = out
+    _device_of(x, Bm, Cm, dt_out)
+    st = _native.load().ssd_mixer_prologue(_desc(xBC), _desc(conv_weight), _desc(conv_bias),
+                                           _desc(conv_state), _desc(conv_windows), _desc(dt),
+                                           _desc(dt_bias), 1 if dt_softplus else 0, ngroups,
+                                           _desc(x), _desc(Bm), _desc(Cm), _desc(dt_out),
+                                           _stream(dev))
+    _native.check(st, "ssd_mixer_prologue")
+    return x, Bm, Cm, dt_out
+
+
 def chunk_cumsum(dt, A, chunk_size, out=None):
     """G [B, H, nc*Q] f32: log2(e) times the in-chunk inclusive cumsum of A*dt."""
     dev = _device_of(dt, A, out)

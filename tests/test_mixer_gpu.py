@@ -1,0 +1,125 @@
+"""GPU parity of the mixer prologue (ssd_mixer_prologue: causal conv1d + SiLU,
+x / B / C split, dt bias + softplus, conv state and windows) against the fp64
+oracle, and of the prologue followed by the scan against the recurrence.
+
+Bars: x, B, C within 2e-2 (bf16 outputs) or 1e-4 (fp32) as max|gpu - ref| /
+max|ref|; dt' within 1e-5 (fp32 softplus of fp32 inputs); the conv state and
+windows are copies of inputs, so they match exactly.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ssd():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from state_space_model_gb300 import build, ssd as mod
+    build.build()
+    return mod
+
+
+def rel(a, b):
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-30))
+
+
+def make_mixer(B, L, H, P, G, N, W, dtype, seed, state=True, bias=True):
+    g = torch.Generator().manual_seed(seed)
+    r = lambda *s: torch.randn(s, generator=g)
+    Dc = H * P + 2 * G * N
+    return dict(xBC=r(B, L, Dc).to(dtype), conv_weight=r(Dc, W) / math.sqrt(W),
+                conv_bias=0.1 * r(Dc) if bias else None,
+                conv_state=r(B, Dc, W).to(dtype) if state else None,
+                dt=r(B, L, H) * 0.5 - 2.0, dt_bias=0.1 * r(H) if bias else None)
+
+
+CASES = [
+    # (B, L, H, P, G, N, W, dtype, state, windows, bias, softplus)
+    (2, 300, 4, 64, 2, 128, 4, torch.bfloat16, True, False, True, True),    # several runs
+    (1, 50, 8, 64, 1, 128, 4, torch.bfloat16, True, True, True, True),      # one run, windows
+    (3, 130, 2, 32, 1, 16, 3, torch.float32, False, False, False, False),
+    (2, 2, 4, 16, 2, 16, 4, torch.bfloat16, True, True, True, True),        # L < W
+    (1, 64, 4, 64, 1, 128, 1, torch.float32, True, True, True, True),       # W = 1, one run
+    (2, 65, 4, 64, 1, 64, 2, torch.bfloat16, True, False, True, False),     # just past a run
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"B{c[0]}L{c[1]}H{c[2]}P{c[3]}G{c[4]}"
+                         f"N{c[5]}W{c[6]}-{str(c[7])[6:]}-st{int(c[8])}win{int(c[9])}")
+def test_mixer_prologue_matches_oracle(ssd, case):
+    B, L, H, P, G, N, W, dtype, state, windows, bias, sp = case
+    inp = make_mixer(B, L, H, P, G, N, W, dtype, seed=L * 7 + W, state=state, bias=bias)
+    out_ref, st_ref, win_ref = orc.causal_conv1d(inp["xBC"], inp["conv_weight"],
+                                                 inp["conv_bias"], inp["conv_state"])
+    x_ref, b_ref, c_ref = orc.split_xbc(out_ref, H, P, G, N)
+    dt_ref = orc.dt_prologue(inp["dt"], inp["dt_bias"], sp)
+    d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    Dc = H * P + 2 * G * N
+    win = torch.empty((B, L, Dc, W), dtype=dtype, device="cuda") if windows else None
+    x, Bm, Cm, dt = ssd.mixer_prologue(d["xBC"], d["conv_weight"], d["dt"], H, P, G, N,
+                                       conv_bias=d["conv_bias"], conv_state=d["conv_state"],
+                                       conv_windows=win, dt_bias=d["dt_bias"], dt_softplus=sp)
+    torch.cuda.synchronize()
+    bar = 2e-2 if dtype == torch.bfloat16 else 1e-4
+    for got, ref in ((x, x_ref), (Bm, b_ref), (Cm, c_ref)):
+        assert got.dtype == dtype
+        assert rel(got.double().cpu().numpy(), ref) <= bar
+    assert rel(dt.double().cpu().numpy(), dt_ref) <= 1e-5
+    cast = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dtype)
+    if state:
+        assert torch.equal(d["conv_state"].cpu(), cast(st_ref))
+    if windows:
+        assert torch.equal(win.cpu(), cast(win_ref))
+
+
+def test_conv_state_carries_across_calls(ssd):
+    """Two calls over the halves of a sequence, the state carried in place,
+    equal one call over the whole sequence bit for bit."""
+    H, P, G, N, W = 4, 64, 1, 128, 4
+    inp = make_mixer(2, 200, H, P, G, N, W, torch.bfloat16, seed=3)
+    d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    st_one = d["conv_state"].clone()
+    whole = ssd.mixer_prologue(d["xBC"], d["conv_weight"], d["dt"], H, P, G, N,
+                               conv_bias=d["conv_bias"], conv_state=st_one, dt_bias=d["dt_bias"])
+    st_two = d["conv_state"].clone()
+    parts = []
+    for lo, hi in ((0, 77), (77, 200)):
+        parts.append(ssd.mixer_prologue(d["xBC"][:, lo:hi].contiguous(), d["conv_weight"],
+                                        d["dt"][:, lo:hi].contiguous(), H, P, G, N,
+                                        conv_bias=d["conv_bias"], conv_state=st_two,
+                                        dt_bias=d["dt_bias"]))
+    torch.cuda.synchronize()
+    for i in range(4):
+        assert torch.equal(whole[i], torch.cat([parts[0][i], parts[1][i]], dim=1))
+    assert torch.equal(st_one, st_two)
+
+
+def test_prologue_then_scan_matches_the_recurrence(ssd):
+    """The mixer's prologue feeding the fused scan: y against the recurrence run on
+    the oracle's own prologue outputs."""
+    B, L, H, P, G, N, W = 2, 512, 8, 64, 2, 128, 4
+    inp = make_mixer(B, L, H, P, G, N, W, torch.bfloat16, seed=9)
+    g = torch.Generator().manual_seed(10)
+    A = -torch.exp(torch.rand(H, generator=g) * math.log(16.0))
+    D = torch.randn(H, generator=g)
+    out_ref, _, _ = orc.causal_conv1d(inp["xBC"], inp["conv_weight"], inp["conv_bias"],
+                                      inp["conv_state"])
+    x_ref, b_ref, c_ref = (torch.from_numpy(np.ascontiguousarray(a))
+                           for a in orc.split_xbc(out_ref, H, P, G, N))
+    dt_ref = torch.from_numpy(orc.dt_prologue(inp["dt"], inp["dt_bias"]))
+    y_ref, fin_ref = orc.recurrence(x_ref, dt_ref, A, b_ref, c_ref, D, None, ngroups=G)
+    d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    x, Bm, Cm, dt = ssd.mixer_prologue(d["xBC"], d["conv_weight"], d["dt"], H, P, G, N,
+                                       conv_bias=d["conv_bias"], conv_state=d["conv_state"],
+                                       dt_bias=d["dt_bias"])
+    y, fin = ssd.chunked_fwd(x, dt, A.cuda(), Bm, Cm, D.cuda(), None, 256, G)
+    torch.cuda.synchronize()
+    assert rel(y.double().cpu().numpy(), y_ref) <= 2e-2
+    assert rel(fin.double().cpu().numpy(), fin_ref) <= 2e-2
