@@ -486,6 +486,8 @@ def main():
     ap.add_argument("--workload", default=gen.HEADLINE, choices=sorted(gen.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gate", action="store_true",
+                    help="prefill: gate the output, y * silu(z) (ssd_chunked_fwd_gated)")
     ap.add_argument("--tokens", type=int, default=1,
                     help="--op ssu: decode tokens per sequence and call (T > 1 keeps the "
                          "per-token state cache)")
@@ -525,10 +527,14 @@ def main():
     fin = torch.empty((B, H, P, N), dtype=torch.float32, device=dev)
     ws = torch.empty(ssd.workspace_size(B, L, H, P, N, w.ngroups, w.chunk_size, w.torch_dtype),
                      dtype=torch.uint8, device=dev)
+    # --gate: the mixer's output gate fused in, y * silu(z) (z ~ N(0, 1), dtype of x)
+    z = (torch.randn((B, L, H, P), generator=torch.Generator().manual_seed(w.seed + 7 + rank))
+         .to(w.torch_dtype).to(dev) if args.gate else None)
+    z_bytes = 0 if z is None else z.numel() * z.element_size()
 
     def step():
         ssd.chunked_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["initial_states"],
-                        w.chunk_size, w.ngroups, y=y, final_states=fin, workspace=ws)
+                        w.chunk_size, w.ngroups, y=y, final_states=fin, workspace=ws, z=z)
 
     clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
@@ -558,11 +564,15 @@ def main():
     fused = plan.startswith("fused")
     reps = max(10, min(args.steps, 200))
     sb = stage_bytes(w)
+    if args.gate and not fused:
+        raise SystemExit("bench.py: --gate times the fused plan; this workload runs four steps")
     if fused:
         # one kernel launch per step: its average duration is the timed region's
         # (events on the launching stream, back-to-back launches)
-        kstats = {"ssd_fused": ms}
-        sb["ssd_fused"] = path_work(w)[0]
+        # (gated: the step is the fused kernel and the gate pass, timed together)
+        kname = "ssd_fused+k_gate" if args.gate else "ssd_fused"
+        kstats = {kname: ms}
+        sb[kname] = path_work(w)[0] + z_bytes
     else:
         # the four stage entry points, events between them
         nc = -(-L // w.chunk_size)
@@ -596,6 +606,7 @@ def main():
                 "peak_source": pk["source"],
                 "kernel_ms_all": {k: round(v, 4) for k, v in kstats.items()}}
     pbytes, pflops = path_work(w)
+    pbytes += z_bytes
     t_roof = max(pbytes / (pk["hbm_gbs"] * 1e9), pflops / (pk["bf16_tflops"] * 1e12))
     path_roof = {"t_roof_us": t_roof * 1e6, "t_step_us": ms * 1e3,
                  "frac": t_roof / (ms / 1e3), "bytes": pbytes, "flops": pflops,
@@ -603,7 +614,7 @@ def main():
 
     # end to end: pinned host inputs -> device, the call, results -> pinned host
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.gate:   # (the gated line is a kernel measurement)
         host = {k: (None if v is None else v.pin_memory()) for k, v in inp_cpu.items()}
         y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
         f_h = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
@@ -649,11 +660,14 @@ def main():
             "config": {"workload": w.name, "batch": B, "seqlen": L, "nheads": H, "headdim": P,
                        "dstate": N, "ngroups": w.ngroups, "chunk_size": w.chunk_size,
                        "initial_states": w.init_states, "parallelism": f"replicas{world}",
+                       **({"gate": "y * silu(z), a second pass after the fused kernel"}
+                          if args.gate else {}),
                        "l2": (f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > "
                               f"{L2_BYTES / 1e6:.0f} MB), no flush")
                        if in_bytes > L2_BYTES else "inputs smaller than L2"},
             "roofline": roofline, "path_roofline": path_roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": (1 if fused else 4) * args.steps, "plan": plan, "clocks": clk,
+            "gpu_launches": ((1 if fused else 4) + (1 if args.gate else 0)) * args.steps,
+            "plan": plan, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

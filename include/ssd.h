@@ -129,6 +129,26 @@ ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt,
                            void *workspace, size_t workspace_bytes,
                            void *stream);
 
+/* The same forward with the mixer's output gate applied to y: "Optimizing
+ * Nemotron v3 Super in TensorRT-LLM", section 6.2 (out * silu(z)), here for
+ * every token of the prefill:
+ *
+ *   y[b, t, h, p] = (the ssd_chunked_fwd output) * silu(z[b, t, h, p]),
+ *   silu(z) = z / (1 + exp(-z))
+ *
+ * z [B, L, H, P] in the dtype of x, 16-byte aligned base, outer strides
+ * multiples of 16 bytes, overlapping no output.  On the fused plan the gate is
+ * applied in the kernel's output stage (z is read once; y is written once); on
+ * the four-step plan by one more launch after chunk_scan.  Everything else as
+ * ssd_chunked_fwd (same workspace size). */
+ssd_status ssd_chunked_fwd_gated(const ssd_tensor *x, const ssd_tensor *dt,
+                                 const ssd_tensor *A, const ssd_tensor *B,
+                                 const ssd_tensor *C, const ssd_tensor *D,
+                                 const ssd_tensor *z, const ssd_tensor *initial_states,
+                                 int64_t chunk_size, int64_t ngroups, ssd_tensor *y,
+                                 ssd_tensor *final_states, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
 /* ---- allocation-free variant ------------------------------------------------
  * The pages have no counterpart of this call; it exists for callers that
  * cannot hand the library a device workspace: code that runs where no

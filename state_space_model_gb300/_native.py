@@ -43,6 +43,7 @@ SIGNATURES = {
     "ssd_workspace_size": [_I64, _I64, _I64, _I64, _I64, _I64, _I64, _I32,
                            ctypes.POINTER(ctypes.c_size_t)],
     "ssd_chunked_fwd": [_T, _T, _T, _T, _T, _T, _T, _I64, _I64, _T, _T, _VP, _SZ, _VP],
+    "ssd_chunked_fwd_gated": [_T, _T, _T, _T, _T, _T, _T, _T, _I64, _I64, _T, _T, _VP, _SZ, _VP],
     "ssd_chunked_fwd_static_scratch": [_T, _T, _T, _T, _T, _T, _T, _I64, _I64, _T, _T, _VP],
     "ssd_device_status": [_VP],
     "ssd_state_update": [_T, _T, _T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _VP],

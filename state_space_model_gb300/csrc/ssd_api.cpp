@@ -346,11 +346,14 @@ ssd_status ssd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int
     return ok();
 }
 
-ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt, const ssd_tensor *A,
-                           const ssd_tensor *Bm, const ssd_tensor *Cm, const ssd_tensor *D,
-                           const ssd_tensor *h0, int64_t chunk_size, int64_t ngroups,
-                           ssd_tensor *y, ssd_tensor *final_states, void *workspace,
-                           size_t workspace_bytes, void *stream) {
+namespace {
+
+// ssd_chunked_fwd (z = NULL) and ssd_chunked_fwd_gated.
+ssd_status chunked_fwd_impl(const ssd_tensor *x, const ssd_tensor *dt, const ssd_tensor *A,
+                            const ssd_tensor *Bm, const ssd_tensor *Cm, const ssd_tensor *D,
+                            const ssd_tensor *z, const ssd_tensor *h0, int64_t chunk_size,
+                            int64_t ngroups, ssd_tensor *y, ssd_tensor *final_states,
+                            void *workspace, size_t workspace_bytes, void *stream) {
     if (!x) return fail(SSD_ERR_INVALID_ARG, "x: null tensor descriptor");
     if (x->ndim != 4) return fail(SSD_ERR_INVALID_ARG, "x: ndim %d, expected 4", x->ndim);
     if (!Bm) return fail(SSD_ERR_INVALID_ARG, "B: null tensor descriptor");
@@ -369,6 +372,7 @@ ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt, const ssd_
     if ((st = check_tensor(Cm, "C", 4, sbc, xdt, false, true))) return st;
     if (D && (st = check_tensor(D, "D", 1, sh, SSD_F32, true, false))) return st;
     if (h0 && (st = check_tensor(h0, "initial_states", 4, sst, SSD_F32, true, true))) return st;
+    if (z && (st = check_tensor(z, "z", 4, sx, xdt, false, true))) return st;
     if ((st = check_tensor(y, "y", 4, sx, xdt, false, true))) return st;
     if (final_states &&
         (st = check_tensor(final_states, "final_states", 4, sst, SSD_F32, true, true)))
@@ -386,11 +390,11 @@ ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt, const ssd_
     }
 
     const Range ins[] = {range_of(x), range_of(dt), range_of(A), range_of(Bm), range_of(Cm),
-                         range_of(D), range_of(h0)};
-    const char *in_names[] = {"x", "dt", "A", "B", "C", "D", "initial_states"};
+                         range_of(D), range_of(h0), range_of(z)};
+    const char *in_names[] = {"x", "dt", "A", "B", "C", "D", "initial_states", "z"};
     const Range ry = range_of(y), rf = range_of(final_states);
     const Range rw = range_raw(workspace, Bn > 0 ? plan.total : 0);
-    for (int i = 0; i < 7; ++i) {
+    for (int i = 0; i < 8; ++i) {
         if (overlap(ry, ins[i])) return fail(SSD_ERR_INVALID_ARG, "y overlaps %s", in_names[i]);
         if (overlap(rf, ins[i]))
             return fail(SSD_ERR_INVALID_ARG, "final_states overlaps %s", in_names[i]);
@@ -404,7 +408,7 @@ ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt, const ssd_
     auto dp = [](const ssd_tensor *t) -> const void * { return t ? t->data : nullptr; };
     if ((st = check_device_ptrs({{dp(x), "x"}, {dp(dt), "dt"}, {dp(A), "A"}, {dp(Bm), "B"},
                                  {dp(Cm), "C"}, {dp(D), "D"}, {dp(h0), "initial_states"},
-                                 {dp(y), "y"}, {dp(final_states), "final_states"},
+                                 {dp(z), "z"}, {dp(y), "y"}, {dp(final_states), "final_states"},
                                  {workspace, "workspace"}})))
         return st;
 
@@ -419,6 +423,12 @@ ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt, const ssd_
     a.h0 = h0 ? static_cast<const float *>(h0->data) : nullptr;
     fill_y(a, y);
     a.final_states = final_states ? static_cast<float *>(final_states->data) : nullptr;
+    if (z) {
+        a.z = z->data;
+        a.z_sb = z->stride[0];
+        a.z_sl = z->stride[1];
+        a.z_sh = z->stride[2];
+    }
     char *ws = static_cast<char *>(workspace);
     a.G = reinterpret_cast<float *>(ws + plan.off_G);
     a.S = reinterpret_cast<float *>(ws + plan.off_S);
@@ -429,6 +439,7 @@ ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt, const ssd_
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (plan.fused) {
         if ((st = cuda_status(ssd::launch_fused(a, s), "fused forward"))) return st;
+        if (z && (st = cuda_status(ssd::launch_gate(a, s), "output gate"))) return st;
         return ok();
     }
     if (L > 0) {
@@ -437,7 +448,29 @@ ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt, const ssd_
     }
     if ((st = cuda_status(ssd::launch_state_passing(a, s), "state_passing"))) return st;
     if (L > 0 && (st = cuda_status(ssd::launch_chunk_scan(a, s), "chunk_scan"))) return st;
+    if (z && L > 0 && (st = cuda_status(ssd::launch_gate(a, s), "output gate"))) return st;
     return ok();
+}
+
+}  // namespace
+
+ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt, const ssd_tensor *A,
+                           const ssd_tensor *Bm, const ssd_tensor *Cm, const ssd_tensor *D,
+                           const ssd_tensor *h0, int64_t chunk_size, int64_t ngroups,
+                           ssd_tensor *y, ssd_tensor *final_states, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    return chunked_fwd_impl(x, dt, A, Bm, Cm, D, nullptr, h0, chunk_size, ngroups, y,
+                            final_states, workspace, workspace_bytes, stream);
+}
+
+ssd_status ssd_chunked_fwd_gated(const ssd_tensor *x, const ssd_tensor *dt, const ssd_tensor *A,
+                                 const ssd_tensor *Bm, const ssd_tensor *Cm, const ssd_tensor *D,
+                                 const ssd_tensor *z, const ssd_tensor *h0, int64_t chunk_size,
+                                 int64_t ngroups, ssd_tensor *y, ssd_tensor *final_states,
+                                 void *workspace, size_t workspace_bytes, void *stream) {
+    if (!z) return fail(SSD_ERR_INVALID_ARG, "z: null tensor descriptor");
+    return chunked_fwd_impl(x, dt, A, Bm, Cm, D, z, h0, chunk_size, ngroups, y, final_states,
+                            workspace, workspace_bytes, stream);
 }
 
 namespace {

@@ -40,6 +40,7 @@ struct Args {
     void *h_prev = nullptr;                   // [B, nc, H, P, N]
     int hprev_dt = DT_F32;
     char *ws = nullptr;                       // workspace base (fused path's tail split)
+    const void *z = nullptr;   int64_t z_sb = 0, z_sl = 0, z_sh = 0;   // output gate, or null
 };
 
 // T decode steps per sequence (ssd_state_update_tokens; ssd_state_update is
@@ -90,6 +91,8 @@ struct MixerArgs {
     void *Co = nullptr;         int64_t c_sb = 0, c_sl = 0, c_sg = 0;
 };
 cudaError_t launch_mixer_prologue(const MixerArgs &a, cudaStream_t stream);
+// y *= silu(z) in place (a.y, a.z with their strides, a.d's B, L, H, P).
+cudaError_t launch_gate(const Args &a, cudaStream_t stream);
 
 // Records the text ssd_last_error_detail() returns on this thread.
 void set_error_detail(const char *fmt, ...);

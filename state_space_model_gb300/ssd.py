@@ -77,10 +77,12 @@ def describe_plan(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size,
 
 
 def chunked_fwd(x, dt, A, B, C, D=None, initial_states=None, chunk_size=256, ngroups=1, *,
-                return_final_states=True, y=None, final_states=None, workspace=None):
+                return_final_states=True, y=None, final_states=None, workspace=None, z=None):
     """SSD chunked forward.  Returns ``(y, final_states)`` (the latter None when
-    ``return_final_states`` is False and no buffer was given)."""
-    dev = _device_of(x, dt, A, B, C, D, initial_states, y, final_states, workspace)
+    ``return_final_states`` is False and no buffer was given).  With ``z``
+    [B,L,H,P] (dtype of x) the output is gated, y * silu(z)
+    (``ssd_chunked_fwd_gated``)."""
+    dev = _device_of(x, dt, A, B, C, D, initial_states, y, final_states, workspace, z)
     lib = _native.load()
     Bn, L, H, P = x.shape
     N = B.shape[-1]
@@ -91,11 +93,18 @@ def chunked_fwd(x, dt, A, B, C, D=None, initial_states=None, chunk_size=256, ngr
     need = workspace_size(Bn, L, H, P, N, ngroups, chunk_size, x.dtype)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    st = lib.ssd_chunked_fwd(_desc(x), _desc(dt), _desc(A), _desc(B), _desc(C), _desc(D),
-                             _desc(initial_states), chunk_size, ngroups, _desc(y),
-                             _desc(final_states), ctypes.c_void_p(workspace.data_ptr()),
-                             workspace.numel() * workspace.element_size(), _stream(dev))
-    _native.check(st, "ssd_chunked_fwd")
+    ws = (ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size())
+    if z is None:
+        st = lib.ssd_chunked_fwd(_desc(x), _desc(dt), _desc(A), _desc(B), _desc(C), _desc(D),
+                                 _desc(initial_states), chunk_size, ngroups, _desc(y),
+                                 _desc(final_states), *ws, _stream(dev))
+        _native.check(st, "ssd_chunked_fwd")
+    else:
+        st = lib.ssd_chunked_fwd_gated(_desc(x), _desc(dt), _desc(A), _desc(B), _desc(C),
+                                       _desc(D), _desc(z), _desc(initial_states), chunk_size,
+                                       ngroups, _desc(y), _desc(final_states), *ws,
+                                       _stream(dev))
+        _native.check(st, "ssd_chunked_fwd_gated")
     return y, final_states
 
 

@@ -123,3 +123,35 @@ def test_prologue_then_scan_matches_the_recurrence(ssd):
     torch.cuda.synchronize()
     assert rel(y.double().cpu().numpy(), y_ref) <= 2e-2
     assert rel(fin.double().cpu().numpy(), fin_ref) <= 2e-2
+
+
+GATED = [
+    # (B, L, H, P, N, G, Q, dtype, h0): fused plan (bf16, P 64, N 128) incl. a ragged
+    # end and a sequence split; four-step plan (fp32, other P / N)
+    (2, 512, 8, 64, 128, 2, 256, torch.bfloat16, False),
+    (1, 300, 4, 64, 128, 1, 128, torch.bfloat16, True),
+    (1, 8000, 4, 64, 128, 2, 256, torch.bfloat16, True),
+    (2, 200, 4, 32, 64, 2, 64, torch.bfloat16, False),
+    (1, 130, 3, 16, 16, 1, 64, torch.float32, True),
+]
+
+
+@pytest.mark.parametrize("case", GATED, ids=lambda c: f"B{c[0]}L{c[1]}H{c[2]}P{c[3]}N{c[4]}"
+                         f"G{c[5]}Q{c[6]}-{str(c[7])[6:]}-h0{int(c[8])}")
+def test_gated_forward_matches_oracle(ssd, case):
+    from state_space_model_gb300 import inputs as gen
+    B, L, H, P, N, G, Q, dtype, h0 = case
+    w = gen.small_case("bf16" if dtype == torch.bfloat16 else "f32", batch=B, seqlen=L,
+                       nheads=H, headdim=P, dstate=N, ngroups=G, chunk_size=Q, init_states=h0)
+    inp = gen.make_inputs(w)
+    z = torch.randn((B, L, H, P), generator=torch.Generator().manual_seed(L)).to(dtype)
+    y_ref, fin_ref = orc.recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                    inp["initial_states"], ngroups=G)
+    yg_ref = orc.gate(y_ref, z)
+    d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    y, fin = ssd.chunked_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"],
+                             d["initial_states"], Q, G, z=z.cuda())
+    torch.cuda.synchronize()
+    bar = 2e-2 if dtype == torch.bfloat16 else 1e-4
+    assert rel(y.double().cpu().numpy(), yg_ref) <= bar
+    assert rel(fin.double().cpu().numpy(), fin_ref) <= bar
