@@ -137,10 +137,9 @@ ssd_status ssd_chunked_fwd(const ssd_tensor *x, const ssd_tensor *dt,
  *   silu(z) = z / (1 + exp(-z))
  *
  * z [B, L, H, P] in the dtype of x, 16-byte aligned base, outer strides
- * multiples of 16 bytes, overlapping no output.  On the fused plan the gate is
- * applied in the kernel's output stage (z is read once; y is written once); on
- * the four-step plan by one more launch after chunk_scan.  Everything else as
- * ssd_chunked_fwd (same workspace size). */
+ * multiples of 16 bytes, overlapping no output.  The gate is one more launch
+ * after the scan (on either plan), in place on y: y read and written, z read
+ * once.  Everything else as ssd_chunked_fwd (same workspace size). */
 ssd_status ssd_chunked_fwd_gated(const ssd_tensor *x, const ssd_tensor *dt,
                                  const ssd_tensor *A, const ssd_tensor *B,
                                  const ssd_tensor *C, const ssd_tensor *D,
