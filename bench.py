@@ -162,6 +162,7 @@ class ClockSampler:
 KERNEL_SOURCES = {
     "ssd_fused": ["ssd_fused.cu", "ptx_sm100.cuh", "ssd_tc.cuh", "ssd_internal.h"],
     "k_ssu_tokens": ["ssd_ssu.cu", "ptx_sm100.cuh", "ssd_internal.h"],
+    "k_conv_prologue": ["ssd_mixer.cu", "ssd_internal.h"],
 }
 
 
@@ -467,7 +468,8 @@ def run_prologue(args, world, rank, local):
                        if in_bytes > L2_BYTES else "xBC smaller than L2"},
             "roofline": {"bound": "hbm", "kernel": "k_conv_prologue", "achieved": achieved,
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-                         "traffic": None, "algorithmic_bytes": nbytes, "kernel_ms": ms,
+                         "traffic": recorded_traffic("k_conv_prologue", f"prologue_{w.name}"),
+                         "algorithmic_bytes": nbytes, "kernel_ms": ms,
                          "peak_source": pk["source"]},
             "gpu_launches": 2 * args.steps, "clocks": clk,
         }
