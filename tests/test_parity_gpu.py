@@ -353,3 +353,22 @@ def test_fused_split_matches_oracle(B, H, L, G):
         for h in range(H):
             assert rel(y[b, :, h], yr[b, :, h]) <= TOL["bf16"]
             assert rel(fin[b, h], fr[b, h]) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("B,H,L,G", [(2, 96, 640, 2), (3, 102, 300, 1)])
+def test_fused_many_slabs_match_oracle(B, H, L, G):
+    """More (batch, head) slabs than SMs (several waves of CTAs, heads and
+    batches mixed within a wave).  Every slab checked; ragged L; initial states
+    and D given."""
+    w = gen.small_case("bf16", batch=B, seqlen=L, nheads=H, ngroups=G, chunk_size=256,
+                       init_states=True, seed=977 + L)
+    plan = ssd().describe_plan(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups,
+                               w.chunk_size, w.torch_dtype)
+    assert plan.startswith("fused") and "segments" not in plan, plan
+    inp = gen.make_inputs(w)
+    y, fin = run(w, inp)
+    yr, fr = oracle_full(w, inp)
+    for b in range(B):
+        for h in range(H):
+            assert rel(y[b, :, h], yr[b, :, h]) <= TOL["bf16"], (b, h)
+            assert rel(fin[b, h], fr[b, h]) <= TOL["bf16"], (b, h)
