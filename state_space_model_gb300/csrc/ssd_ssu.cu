@@ -13,13 +13,13 @@
 // The step reads and writes the fp32 state once per call, whatever T, and
 // everything else is a few hundred bytes per head and token, so it is bound
 // by HBM.  Each CTA owns a tile of state rows of one (batch, head): one
-// elected thread brings the whole tile into shared memory with bulk copies
-// (the bytes in flight cost no registers, so an SM keeps several tiles in
-// flight), every thread then takes four consecutive columns of its rows into
-// registers, runs the T tokens there, and writes the cached and final
-// states with coalesced 16-byte stores.  A row's output is a shuffle
-// reduction over the lanes holding it.  No tensor cores: the only
-// contraction is a length-N dot product per row.
+// elected thread brings the whole tile into shared memory with bulk copies,
+// the T tokens update it there in place (each thread four consecutive
+// columns of its rows), and one bulk copy writes it back, so neither
+// direction holds registers and an SM keeps six tiles in flight.  The
+// per-token state cache is written with coalesced 16-byte stores.  A row's
+// output is a shuffle reduction over the lanes holding it.  No tensor cores:
+// the only contraction is a length-N dot product per row.
 #include "ptx_sm100.cuh"
 #include "ssd_internal.h"
 #include "ssd_tc.cuh"
@@ -31,9 +31,17 @@ namespace ssd {
 namespace {
 
 constexpr int kSsuThreads = 128;
-constexpr int kMaxRT = 16;                 // rows per thread at most (64 fp32 registers)
+constexpr int kMaxRT = 16;                 // passes of rows per tile at most (32 KB at N = 128)
 constexpr uint32_t kBulkChunk = 16384;     // bytes per bulk copy
 constexpr unsigned kErrTimeout = 1u;       // same bit as the fused forward's
+
+// Shared -> global bulk copy of `bytes` (16-byte aligned addresses, a multiple
+// of 16 bytes), tracked by this thread's bulk-async group.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(ptx::smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
 
 template <typename T>
 __device__ __forceinline__ float to_f(T v);
@@ -69,7 +77,7 @@ __device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
 // Each token's x and z values of the tile's rows are staged in shared memory
 // (double-buffered by token parity) so no row waits on its own global load.
 template <int N, typename T>
-__global__ void __launch_bounds__(kSsuThreads, 5)
+__global__ void __launch_bounds__(kSsuThreads)
 k_ssu_tokens(const SsuArgs a, int rows, unsigned int *err) {
     constexpr int kTpr = N / 4;                     // threads per state row
     constexpr int kRowsPass = kSsuThreads / kTpr;   // rows per pass
@@ -116,11 +124,6 @@ k_ssu_tokens(const SsuArgs a, int rows, unsigned int *err) {
         if (threadIdx.x == 0) atomicOr(err, kErrTimeout);
         return;
     }
-    float4 s[kMaxRT];
-#pragma unroll
-    for (int i = 0; i < kMaxRT; ++i)
-        if (i < nrt && rr + i * kRowsPass < rows) s[i] = tile[(rr + i * kRowsPass) * kTpr + c];
-
     for (int t = 0; t < a.T; ++t) {
         float d = a.dt[int64_t(b) * a.dt_sb + int64_t(t) * a.dt_st + h] + bias;
         const int64_t bc = int64_t(b) * a.bc_sb + int64_t(t) * a.bc_st + int64_t(g) * a.bc_sg + 4 * c;
@@ -128,14 +131,16 @@ k_ssu_tokens(const SsuArgs a, int rows, unsigned int *err) {
         const float4 cq = load4(static_cast<const T *>(a.Cm) + bc);
         if (a.parent && t > 0) {
             // start from the state after the parent token, when it is an earlier one
+            // (each thread reloads its own entries of the tile)
             const int pt = a.parent[int64_t(b) * a.par_sb + t];
             if (pt >= 0 && pt < t) {
                 const float *src = a.inter + ((int64_t(b) * a.T + pt) * a.H + h) * a.P * N;
-#pragma unroll
-                for (int i = 0; i < kMaxRT; ++i)
-                    if (i < nrt && rr + i * kRowsPass < rows)
-                        s[i] = *reinterpret_cast<const float4 *>(
-                            src + int64_t(r0 + rr + i * kRowsPass) * N + 4 * c);
+                for (int i = 0; i < nrt; ++i) {
+                    const int lr = rr + i * kRowsPass;
+                    if (lr < rows)
+                        tile[lr * kTpr + c] = *reinterpret_cast<const float4 *>(
+                            src + int64_t(r0 + lr) * N + 4 * c);
+                }
             }
         }
         if (a.softplus) d = d <= 20.f ? log1pf(expf(d)) : d;   // log(1 + e^d), = d to fp32 above 20
@@ -146,21 +151,22 @@ k_ssu_tokens(const SsuArgs a, int rows, unsigned int *err) {
         T *orow = static_cast<T *>(a.out) + int64_t(b) * a.o_sb + int64_t(t) * a.o_st +
                   int64_t(h) * a.o_sh + r0;
         float *ir = a.inter ? a.inter + ((int64_t(b) * a.T + t) * a.H + h) * a.P * N : nullptr;
-#pragma unroll
-        for (int i = 0; i < kMaxRT; ++i) {
-            if (i >= nrt) break;
+#pragma unroll 4
+        for (int i = 0; i < nrt; ++i) {
             const int lr = rr + i * kRowsPass;        // local row
             const bool live = lr < rows;              // false only when P < kRowsPass
             float xv = 0.f, partial = 0.f;
             if (live) {
                 xv = xt[lr];
                 const float u = d * xv;
-                s[i].x = fmaf(s[i].x, dA, u * bq.x);
-                s[i].y = fmaf(s[i].y, dA, u * bq.y);
-                s[i].z = fmaf(s[i].z, dA, u * bq.z);
-                s[i].w = fmaf(s[i].w, dA, u * bq.w);
-                if (ir) *reinterpret_cast<float4 *>(ir + int64_t(r0 + lr) * N + 4 * c) = s[i];
-                partial = fmaf(s[i].x, cq.x, fmaf(s[i].y, cq.y, fmaf(s[i].z, cq.z, s[i].w * cq.w)));
+                float4 v = tile[lr * kTpr + c];
+                v.x = fmaf(v.x, dA, u * bq.x);
+                v.y = fmaf(v.y, dA, u * bq.y);
+                v.z = fmaf(v.z, dA, u * bq.z);
+                v.w = fmaf(v.w, dA, u * bq.w);
+                tile[lr * kTpr + c] = v;
+                if (ir) *reinterpret_cast<float4 *>(ir + int64_t(r0 + lr) * N + 4 * c) = v;
+                partial = fmaf(v.x, cq.x, fmaf(v.y, cq.y, fmaf(v.z, cq.z, v.w * cq.w)));
             }
             // sum over the row's kTpr lanes (contiguous within the warp)
 #pragma unroll
@@ -177,10 +183,17 @@ k_ssu_tokens(const SsuArgs a, int rows, unsigned int *err) {
         }
     }
     if (a.update) {
-#pragma unroll
-        for (int i = 0; i < kMaxRT; ++i)
-            if (i < nrt && rr + i * kRowsPass < rows)
-                __stcs(reinterpret_cast<float4 *>(st) + (rr + i * kRowsPass) * kTpr + c, s[i]);
+        // every thread's tile writes, then one bulk copy back (its shared-memory
+        // reads must finish before the CTA leaves)
+        ptx::fence_proxy_async_smem();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (uint32_t off = 0; off < bytes; off += kBulkChunk)
+                bulk_store(reinterpret_cast<char *>(st) + off, reinterpret_cast<char *>(tile) + off,
+                           bytes - off < kBulkChunk ? bytes - off : kBulkChunk);
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group_read0();
+        }
     }
 }
 
@@ -197,7 +210,7 @@ int sm_count() {
 template <int N, typename T>
 cudaError_t launch_n(const SsuArgs &a, cudaStream_t s) {
     constexpr int kRowsPass = kSsuThreads / (N / 4);
-    // the largest tile a thread's registers hold, halved while the grid is
+    // tiles of at most kMaxRT passes of rows (32 KB at N = 128), halved while the grid is
     // below two CTAs per SM (few sequences: spread the rows over more SMs)
     int rows = a.P < kMaxRT * kRowsPass ? a.P : kMaxRT * kRowsPass;   // P / rows whole
     const int64_t want = 2 * int64_t(sm_count());
