@@ -515,8 +515,29 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             const int k0 = states_only ? nblk : 0;
             int k_s = 0, k_in = k0, k_a = k0, k_cb = k0;   // next block of each product
             uint64_t idle_since = 0;
+            // Each pass checks the products in the order L x, B^T (w o x), C h^T,
+            // C B^T and issues every one that is ready (an issue takes about as
+            // long as the product runs); measured the fastest of the orders tried.
             while (states_only ? k_s < nblk : (k_in < nblk || k_a < nblk)) {
                 bool progress = false;
+                // L x(k): the decay operand is built (after S^T(k) in issue order, so
+                // that intra_done also covers S^T)
+                if (k_a < k_cb && k_a < k_s) {
+                    const int s = k_a & 1;
+                    const uint32_t par = (k_a >> 1) & 1;
+                    if (ptx::mbar_test_wait(&L_ready[s], par)) {
+                        ptx::tc_fence_after();
+                        const uint64_t x0 = dX + uint64_t((k_a % 3) * 1024);
+                        const uint32_t t_l = tmem + 128 * s;
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            ptx::mma_bf16_ts(t_l + 64, t_l + ks * 8, x0 + uint64_t(ks * 128), kIdKmn,
+                                             ks != 0);
+                        ptx::mma_commit(&intra_done[s]);
+                        ++k_a;
+                        progress = true;
+                    }
+                }
                 // S^T(k) = B^T (w o x): w o x written, B landed, and S^T(k - 2)
                 // absorbed into the state
                 if (k_s < nblk) {
@@ -550,24 +571,6 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                                              dHB + uint64_t(ks * 128), kIdKmn, ks != 0);
                         ptx::mma_commit(&inter_done[s]);
                         ++k_in;
-                        progress = true;
-                    }
-                }
-                // L x(k): the decay operand is built (after S^T(k) in issue order, so
-                // that intra_done also covers S^T)
-                if (k_a < k_cb && k_a < k_s) {
-                    const int s = k_a & 1;
-                    const uint32_t par = (k_a >> 1) & 1;
-                    if (ptx::mbar_test_wait(&L_ready[s], par)) {
-                        ptx::tc_fence_after();
-                        const uint64_t x0 = dX + uint64_t((k_a % 3) * 1024);
-                        const uint32_t t_l = tmem + 128 * s;
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks)
-                            ptx::mma_bf16_ts(t_l + 64, t_l + ks * 8, x0 + uint64_t(ks * 128), kIdKmn,
-                                             ks != 0);
-                        ptx::mma_commit(&intra_done[s]);
-                        ++k_a;
                         progress = true;
                     }
                 }
