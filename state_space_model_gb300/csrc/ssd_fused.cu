@@ -427,8 +427,9 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         for (int j = 0; j < 4; ++j) fetch_dt(j);
         // the states-only pass needs no C
         int kb = 0, kc = states_only ? nblk : 0, kx = 0, kr = 0;   // next block of each stream
+        const int kx_end = states_only ? nblk : (nblk < 3 ? nblk : 3);
         uint64_t idle_since = 0;
-        while (kb < nblk || kc < nblk || kx < nblk || kr < nblk) {
+        while (kb < nblk || kc < nblk || kx < kx_end || kr < nblk) {
             int fired = 0;   // bit i: stream i issued (lane 0's decision)
             if (lane == 0) {
                 // B: read by C B^T(k - 2) and B^T (w o x)(k - 2)
@@ -458,8 +459,10 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                         fired |= 2;
                     }
                 }
-                // x: its slot holds y(k - 3) until that tile's store has read it
-                if (kx < nblk) {
+                // x: its slot holds y(k - 3) until that tile's store has read it;
+                // past the first three blocks the storer of y(k - 3) issues x(k)
+                // itself (the states-only pass has no y)
+                if (kx < (states_only ? nblk : (nblk < 3 ? nblk : 3))) {
                     const int slot = kx % 3;
                     if (kx < 3 || ptx::mbar_test_wait(&xfree[slot], ((kx / 3) - 1) & 1)) {
                         const int t0 = int(t_begin + int64_t(kx) * 128);
@@ -825,7 +828,11 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 ptx::tma_store_4d(&tm_y, tile, 0, h, int(t_begin + int64_t(k) * 128), b);
                 ptx::bulk_commit_group();
                 ptx::bulk_wait_group_read0();   // the slot takes x(k + 3) next
-                ptx::mbar_arrive(&xfree[k % 3]);
+                if (k + 3 < nblk) {
+                    ptx::mbar_arrive_expect_tx(&full_X[k % 3], 16384);
+                    ptx::tma_load_4d(tile, &tm_x, &full_X[k % 3], 0, h,
+                                     int(t_begin + int64_t(k + 3) * 128), b);
+                }
             }
         }
         if (storer) ptx::bulk_wait_group0();
