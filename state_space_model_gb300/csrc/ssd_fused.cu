@@ -205,20 +205,20 @@ __device__ __forceinline__ void l_block(const uint32_t (&v)[32], int col0, bool 
 __device__ __forceinline__ void build_record(const float (&dt)[4], float Ah, int lane,
                                              float *rec) {
     float tot[4], own[4];
+    // inclusive scans of the four 32-row quarters, interleaved; a quarter's
+    // total is its last lane's scan value
 #pragma unroll
-    for (int qq = 0; qq < 4; ++qq) {
-        const float a = Ah * dt[qq];
-        float v = a, c = a;
+    for (int qq = 0; qq < 4; ++qq) own[qq] = Ah * dt[qq];
 #pragma unroll
-        for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    for (int off = 1; off < 32; off <<= 1) {
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float o = __shfl_up_sync(0xffffffffu, c, off);
-            if (lane >= off) c += o;
+        for (int qq = 0; qq < 4; ++qq) {
+            const float o = __shfl_up_sync(0xffffffffu, own[qq], off);
+            if (lane >= off) own[qq] += o;
         }
-        tot[qq] = v;
-        own[qq] = c;
     }
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) tot[qq] = __shfl_sync(0xffffffffu, own[qq], 31);
     float pre = 0.f;
 #pragma unroll
     for (int qq = 0; qq < 4; ++qq) {
