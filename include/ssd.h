@@ -89,6 +89,14 @@ const char *ssd_last_error_detail(void);
  * entry point that synchronises; call it where a check is wanted. */
 ssd_status ssd_device_status(void *stream);
 
+/* Test hook for the failure path above: launches one CTA on `stream` whose
+ * bounded wait (on an mbarrier phase nothing completes) gives up after
+ * limit_ns (at most 100 ms) and records the timeout in the device error word,
+ * the same way every kernel of the library does.  The next ssd_device_status
+ * on that stream then returns SSD_ERR_TIMEOUT and clears the word.  Nothing
+ * else is in flight in that CTA, so the context stays usable. */
+ssd_status ssd_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
 /* Bytes of device workspace ssd_chunked_fwd needs for this problem, written
  * to *bytes.  x_dtype is the ssd_dtype of x, B, C.  On the four-step path the
  * workspace holds the scaled in-chunk cumulative sums G [B, H, nc*Q] f32, the

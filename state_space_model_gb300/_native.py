@@ -46,6 +46,7 @@ SIGNATURES = {
     "ssd_chunked_fwd_gated": [_T, _T, _T, _T, _T, _T, _T, _T, _I64, _I64, _T, _T, _VP, _SZ, _VP],
     "ssd_chunked_fwd_static_scratch": [_T, _T, _T, _T, _T, _T, _T, _I64, _I64, _T, _T, _VP],
     "ssd_device_status": [_VP],
+    "ssd_selftest_wait_timeout": [ctypes.c_uint64, _VP],
     "ssd_state_update": [_T, _T, _T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _VP],
     "ssd_state_update_tokens": [_T, _T, _T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _T, _T, _I32,
                                 _VP],

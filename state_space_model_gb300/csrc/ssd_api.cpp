@@ -331,6 +331,13 @@ ssd_status ssd_device_status(void *stream) {
     return ok();
 }
 
+ssd_status ssd_selftest_wait_timeout(uint64_t limit_ns, void *stream) {
+    if (limit_ns > 100000000ull)
+        return fail(SSD_ERR_INVALID_ARG, "limit %llu ns above 100 ms", (unsigned long long)limit_ns);
+    return cuda_status(ssd::launch_wait_selftest(limit_ns, static_cast<cudaStream_t>(stream)),
+                       "wait self-test");
+}
+
 ssd_status ssd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
                               int64_t dstate, int64_t ngroups, int64_t chunk_size,
                               int32_t x_dtype, size_t *bytes) {

@@ -91,6 +91,8 @@ struct MixerArgs {
     void *Co = nullptr;         int64_t c_sb = 0, c_sl = 0, c_sg = 0;
 };
 cudaError_t launch_mixer_prologue(const MixerArgs &a, cudaStream_t stream);
+// One CTA whose wait on an mbarrier nobody arrives at gives up after limit_ns.
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
 // y *= silu(z) in place (a.y, a.z with their strides, a.d's B, L, H, P).
 cudaError_t launch_gate(const Args &a, cudaStream_t stream);
 

@@ -338,3 +338,8 @@ def test_state_update_tokens_error_paths(lib):
                 Bm=e((Bn, 0, G, N), BF16, Bm), Cm=e((Bn, 0, G, N), BF16, Cm),
                 out=e((Bn, 0, H, P), BF16, out), inter=e((Bn, 0, H, P, N), F32, inter),
                 parent=e((Bn, 0), I32, parent)) == 0
+
+
+def test_selftest_wait_limit_is_checked_on_the_host(lib):
+    assert lib.ssd_selftest_wait_timeout(200_000_000, None) == 1
+    assert "100 ms" in detail(lib)
