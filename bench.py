@@ -291,11 +291,13 @@ def cpu_baseline(w, inp):
 SSU_METRIC = "SSU decode tokens/s at the Nemotron hybrid layer shape; % of HBM roofline"
 
 
-def ssu_bytes(Bn, H, P, N, G, T=1, cached=False):
-    """Compulsory HBM bytes of one decode call of T tokens: the fp32 state read
-    and written once, the per-token state cache written when kept, and per
-    token x, z and out (bf16), B and C (bf16), dt (f32); plus A, D, dt_bias."""
-    return 2 * Bn * H * P * N * 4 + (T * Bn * H * P * N * 4 if cached else 0) + \
+def ssu_bytes(Bn, H, P, N, G, T=1, cached=False, state_bytes=4):
+    """Compulsory HBM bytes of one decode call of T tokens: the state (fp32, or
+    bf16 with state_bytes = 2) read and written once, the per-token state cache
+    written when kept, and per token x, z and out (bf16), B and C (bf16), dt
+    (f32); plus A, D, dt_bias."""
+    sb = state_bytes
+    return 2 * Bn * H * P * N * sb + (T * Bn * H * P * N * sb if cached else 0) + \
         T * (3 * Bn * H * P * 2 + 2 * Bn * G * N * 2 + Bn * H * 4) + 3 * H * 4
 
 
@@ -318,22 +320,35 @@ def run_ssu(args, world, rank, local):
     Bn, H, P, N, G = sh["batch"], sh["nheads"], sh["headdim"], sh["dstate"], sh["ngroups"]
     T = args.tokens
     cpu = gen.make_ssu_inputs(Bn, H, P, N, G, seed=20270 + rank, tokens=T if T > 1 else None)
+    sdt = torch.bfloat16 if args.state_dtype == "bf16" else torch.float32
+    sbytes = 2 if args.state_dtype == "bf16" else 4
+    cpu["state"] = cpu["state"].to(sdt)
     d = {k: (None if v is None else v.to(dev)) for k, v in cpu.items()}
+    # the state must not stay in L2 from one call to the next: calls rotate over
+    # nbuf state buffers (other sequences' states) holding together at least
+    # twice L2
+    sbytes_all = Bn * H * P * N * sbytes
+    nbuf = min(8, max(1, -(-2 * L2_BYTES // sbytes_all)))
+    states = [d["state"]] + [d["state"].clone() for _ in range(nbuf - 1)]
     if T > 1:
         out = torch.empty((Bn, T, H, P), dtype=torch.bfloat16, device=dev)
-        inter = torch.empty((Bn, T, H, P, N), dtype=torch.float32, device=dev)
+        inter = torch.empty((Bn, T, H, P, N), dtype=sdt, device=dev)
 
-        def step():
-            ssd.state_update_tokens(d["state"], d["x"], d["dt"], d["A"], d["B"], d["C"],
+        def call(st):
+            ssd.state_update_tokens(st, d["x"], d["dt"], d["A"], d["B"], d["C"],
                                     D=d["D"], z=d["z"], dt_bias=d["dt_bias"], dt_softplus=True,
                                     ngroups=G, intermediate_states=inter, out=out)
     else:
         out = torch.empty((Bn, H, P), dtype=torch.bfloat16, device=dev)
 
-        def step():
-            ssd.state_update(d["state"], d["x"], d["dt"], d["A"], d["B"], d["C"], D=d["D"],
+        def call(st):
+            ssd.state_update(st, d["x"], d["dt"], d["A"], d["B"], d["C"], D=d["D"],
                              z=d["z"], dt_bias=d["dt_bias"], dt_softplus=True, ngroups=G,
                              out=out)
+
+    def step():
+        for st in states:
+            call(st)
 
     # a decode step is a few microseconds of GPU work at small batch, less than
     # the Python call that launches it: replay it from a CUDA graph, as a
@@ -363,13 +378,15 @@ def run_ssu(args, world, rank, local):
     torch.cuda.synchronize()
     clocks.mark_off()
     barrier(world)
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / (args.steps * nbuf), world)   # per call
     clk = clocks.stop()
     pk = peaks()
-    nbytes = ssu_bytes(Bn, H, P, N, G, T, cached=T > 1)
+    nbytes = ssu_bytes(Bn, H, P, N, G, T, cached=T > 1, state_bytes=sbytes)
     wname = "ssu_decode" if T == 1 else f"ssu_decode_{T}_tokens"
     if Bn != gen.SSU_SHAPE["batch"]:
         wname += f"_b{Bn}"
+    if sbytes == 2:
+        wname += "_bf16_state"
     achieved = nbytes / (ms / 1e3) / 1e9
     if rank == 0:
         line = {
@@ -377,18 +394,21 @@ def run_ssu(args, world, rank, local):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded; see state_space_model_gb300/inputs.py)",
-            "config": {"workload": wname,
+            "config": {"workload": wname, "state_dtype": args.state_dtype,
                        "batch": Bn, "tokens": T, "nheads": H, "headdim": P,
                        "dstate": N, "ngroups": G, "gated": True, "dt_softplus": True,
                        "state_cache": T > 1,
-                       "l2": f"state {Bn * H * P * N * 4 / 1e6:.0f} MB, larger than L2"
-                       if Bn * H * P * N * 4 > L2_BYTES else "state smaller than L2"},
+                       "l2": f"calls rotate over {nbuf} state buffer(s) of "
+                             f"{sbytes_all / 1e6:.0f} MB, {nbuf * sbytes_all / 1e6:.0f} MB "
+                             f"together, at least twice L2"},
             "roofline": {"bound": "hbm", "kernel": "k_ssu_tokens", "achieved": achieved,
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                          "traffic": recorded_traffic("k_ssu_tokens", wname),
                          "algorithmic_bytes": nbytes, "kernel_ms": ms,
                          "peak_source": pk["source"]},
-            "gpu_launches": args.steps, "launch": "CUDA graph replay, one kernel per step",
+            "gpu_launches": args.steps * nbuf,
+            "launch": f"CUDA graph replay of {nbuf} call(s), one kernel per call; "
+                      "ms_per_step is per call",
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
@@ -493,6 +513,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=1,
                     help="--op ssu: decode tokens per sequence and call (T > 1 keeps the "
                          "per-token state cache)")
+    ap.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32",
+                    help="--op ssu: dtype the decode state is kept in")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (a smaller case of the same shape)")
     ap.add_argument("--ref-seconds", type=float, default=150.0,

@@ -201,13 +201,17 @@ ssd_status ssd_chunked_fwd_static_scratch(const ssd_tensor *x, const ssd_tensor 
  *   out *= silu(z[b, h]) = z / (1 + exp(-z))        (if z is given)
  *
  * Shapes, dtypes and layouts:
- *   state [B, H, P, N] f32, packed, read and updated in place
+ *   state [B, H, P, N] f32 or bf16, packed, read and updated in place
  *   x     [B, H, P] bf16 or f32                  z   [B, H, P] dtype of x, optional
  *   dt    [B, H] f32 (post-softplus unless dt_softplus, then raw)
  *   A     [H] f32 (<= 0)                         D, dt_bias [H] f32, optional
  *   B, C  [B, G, N] dtype of x, same strides     out [B, H, P] dtype of x
  * The state is the one ssd_chunked_fwd returns as final_states, so prefill
- * followed by decode steps continues the same recurrence.  P and N in
+ * followed by decode steps continues the same recurrence.  A bf16 state is the
+ * 16-bit state cache of the same page's section 6.4.3 (the layout it dispatches
+ * to on Blackwell): the update and out are computed in fp32 from the stored
+ * values, out from the unrounded new state, and the state is stored rounded to
+ * nearest even (the state's dtype is the storage format only).  P and N in
  * {16, 32, 64, 128}; H a multiple of G.  Alignment: state, B and C base
  * pointers 16-byte aligned, B and C outer strides multiples of 16 bytes.
  * Aliasing: out must not overlap any input or the state, and the state must
@@ -244,11 +248,13 @@ ssd_status ssd_state_update(ssd_tensor *state, const ssd_tensor *x, const ssd_te
  * promoted by the caller).
  *
  * Shapes, dtypes and layouts (the token axis second):
- *   state [B, H, P, N] f32, packed
+ *   state [B, H, P, N] f32 or bf16, packed (bf16: rounded as for ssd_state_update,
+ *         after every token: the s of the next token is the rounded one)
  *   x, z, out [B, T, H, P] bf16 or f32 (z optional, out the dtype of x)
  *   dt    [B, T, H] f32                          A, D, dt_bias [H] f32
  *   B, C  [B, T, G, N] dtype of x, same strides
- *   intermediate_states [B, T, H, P, N] f32, packed, optional (required with parent)
+ *   intermediate_states [B, T, H, P, N] dtype of the state, packed, optional
+ *         (required with parent)
  *   parent [B, T] SSD_I32, optional
  * T = 1 without intermediate states or parents is ssd_state_update.  Alignment
  * as for ssd_state_update, plus intermediate_states 16-byte aligned.  Aliasing:

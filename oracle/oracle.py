@@ -321,8 +321,19 @@ def ssu_step(state, x, dt, A, Bm, Cm, D=None, z=None, dt_bias=None, dt_softplus=
     return out, new
 
 
+def _round_state(a, state_dtype):
+    """A state as kept in memory: float64 values rounded to the state's storage
+    dtype ("f32" or "bf16", round to nearest even) and widened back."""
+    t = torch.from_numpy(np.asarray(a, dtype=np.float64))
+    if state_dtype == "bf16":
+        return t.to(torch.bfloat16).to(torch.float64).numpy()
+    if state_dtype == "f32":
+        return t.to(torch.float32).to(torch.float64).numpy()
+    raise ValueError(f"oracle: state dtype {state_dtype!r}")
+
+
 def ssu_tokens(state, x, dt, A, Bm, Cm, D=None, z=None, dt_bias=None, dt_softplus=False,
-               ngroups=1, parent=None, update_state=True):
+               ngroups=1, parent=None, update_state=True, state_dtype=None):
     """T decode steps per sequence, in float64, as one would apply them one
     token at a time -- the multi-token state update of "Optimizing Nemotron
     v3 Super in TensorRT-LLM", section 10.4, with the intermediate-state cache
@@ -336,6 +347,11 @@ def ssu_tokens(state, x, dt, A, Bm, Cm, D=None, z=None, dt_bias=None, dt_softplu
     Returns ``(out [B,T,H,P], final [B,H,P,N], cache [B,T,H,P,N])``: cache[:, t]
     is the state after token t; final is the running state after the last
     token, or the input state unchanged when ``update_state`` is false.
+
+    ``state_dtype`` ("f32" or "bf16") models a state kept in that dtype: each
+    token's update is computed from the kept state in float64 and its output
+    from the unrounded result, and the state is then kept rounded (the running
+    state, the cache and the final state alike).  None keeps float64 throughout.
     """
     f = lambda t: None if t is None else _as_cpu(t).to(torch.float64)
     st0 = f(state)
@@ -355,6 +371,8 @@ def ssu_tokens(state, x, dt, A, Bm, Cm, D=None, z=None, dt_bias=None, dt_softplu
             o, new = ssu_step(run, xv[b:b + 1, t], dtv[b:b + 1, t], A, Bv[b:b + 1, t],
                               Cv[b:b + 1, t], D=D, z=None if zv is None else zv[b:b + 1, t],
                               dt_bias=dt_bias, dt_softplus=dt_softplus, ngroups=ngroups)
+            if state_dtype is not None:
+                new = _round_state(new, state_dtype)
             out[b, t] = o[0]
             cache[b, t] = new[0]
             run = torch.from_numpy(new)

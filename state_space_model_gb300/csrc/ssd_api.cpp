@@ -528,7 +528,8 @@ ssd_status state_update_impl(bool tokens, ssd_tensor *state, const ssd_tensor *x
     const int64_t *sx = tokens ? sx4 : sx3, *sdt = tokens ? sdt3 : sdt2,
                   *sbc = tokens ? sbc4 : sbc3;
     ssd_status st;
-    if ((st = check_tensor(state, "state", 4, sst, SSD_F32, true, true))) return st;
+    // the state is kept in f32 or bf16; its cache in the same dtype
+    if ((st = check_tensor(state, "state", 4, sst, -1, true, true))) return st;
     if ((st = check_tensor(x, "x", 3 + k, sx, -1, false, false))) return st;
     if ((st = check_tensor(dt, "dt", 2 + k, sdt, SSD_F32, false, false))) return st;
     if ((st = check_tensor(A, "A", 1, sh, SSD_F32, true, false))) return st;
@@ -541,7 +542,8 @@ ssd_status state_update_impl(bool tokens, ssd_tensor *state, const ssd_tensor *x
     if (z && (st = check_tensor(z, "z", 3 + k, sx, xdt, false, false))) return st;
     if (dt_bias && (st = check_tensor(dt_bias, "dt_bias", 1, sh, SSD_F32, true, false))) return st;
     if ((st = check_tensor(out, "out", 3 + k, sx, xdt, false, false))) return st;
-    if (inter && (st = check_tensor(inter, "intermediate_states", 5, sin, SSD_F32, true, true)))
+    if (inter &&
+        (st = check_tensor(inter, "intermediate_states", 5, sin, state->dtype, true, true)))
         return st;
     if (parent && (st = check_tensor(parent, "parent", 2, spar, SSD_I32, false, false)))
         return st;
@@ -581,7 +583,8 @@ ssd_status state_update_impl(bool tokens, ssd_tensor *state, const ssd_tensor *x
     a.xdt = xdt;
     a.softplus = dt_softplus ? 1 : 0;
     a.update = update_state ? 1 : 0;
-    a.state = static_cast<float *>(state->data);
+    a.sdt = state->dtype == SSD_BF16 ? ssd::DT_BF16 : ssd::DT_F32;
+    a.state = state->data;
     a.x = x->data;
     a.x_sb = x->stride[0];
     a.x_st = sT(x);
@@ -605,7 +608,7 @@ ssd_status state_update_impl(bool tokens, ssd_tensor *state, const ssd_tensor *x
     a.o_sb = out->stride[0];
     a.o_st = sT(out);
     a.o_sh = sAt(out, 1);
-    a.inter = inter ? static_cast<float *>(inter->data) : nullptr;
+    a.inter = inter ? inter->data : nullptr;
     a.parent = parent ? static_cast<const int32_t *>(parent->data) : nullptr;
     a.par_sb = parent ? parent->stride[0] : 0;
     return cuda_status(ssd::launch_ssu(a, static_cast<cudaStream_t>(stream)), "state update");

@@ -52,7 +52,8 @@ struct SsuArgs {
     int xdt = DT_BF16;                        // dtype of x, B, C, z, out
     int softplus = 0;
     int update = 1;                           // write the final state back
-    float *state = nullptr;
+    int sdt = DT_F32;                         // dtype of state and inter
+    void *state = nullptr;
     const void *x = nullptr;   int64_t x_sb = 0, x_st = 0, x_sh = 0;
     const float *dt = nullptr; int64_t dt_sb = 0, dt_st = 0;
     const float *A = nullptr;
@@ -62,7 +63,7 @@ struct SsuArgs {
     const void *Cm = nullptr;  int64_t bc_sb = 0, bc_st = 0, bc_sg = 0;   // B, C share strides
     const void *z = nullptr;   int64_t z_sb = 0, z_st = 0, z_sh = 0;     // may be null
     void *out = nullptr;       int64_t o_sb = 0, o_st = 0, o_sh = 0;
-    float *inter = nullptr;                   // may be null (not cached)
+    void *inter = nullptr;                    // may be null (not cached)
     const int32_t *parent = nullptr;          // may be null (a chain)
     int64_t par_sb = 0;
 };

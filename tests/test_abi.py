@@ -273,7 +273,8 @@ def test_state_update_error_paths(lib):
     assert call(G=3) == 1 and "ngroups" in detail(lib)
     assert call(state=tens((Bn, H, 48, N), F32, ptr=base)) == 2 and "headdim" in detail(lib)
     assert call(state=tens((Bn, H, P, 256), F32, ptr=base)) == 2 and "dstate" in detail(lib)
-    assert call(state=tens((Bn, H, P, N), BF16, ptr=base)) == 1 and "dtype" in detail(lib)
+    # f32 and bf16 states pass the host checks; int32 does not
+    assert call(state=tens((Bn, H, P, N), 2, ptr=base)) == 1 and "dtype" in detail(lib)
     assert call(dt=tens((Bn, H + 1), F32, ptr=dt.data)) == 1 and "shape" in detail(lib)
     assert call(Cm=tens((Bn, G, N), F32, ptr=Cm.data)) == 1
     # non-contiguous state, misaligned B
@@ -327,6 +328,10 @@ def test_state_update_tokens_error_paths(lib):
     assert call(x=tens((Bn, H, P), BF16, ptr=x.data)) == 1 and "ndim" in detail(lib)
     assert call(dt=tens((Bn, T + 1, H), F32, ptr=dt.data)) == 1 and "shape" in detail(lib)
     assert call(inter=tens((Bn, T, H, P, N), BF16, ptr=inter.data)) == 1
+    # a bf16 state keeps its cache in bf16 too
+    sb = tens((Bn, H, P, N), BF16, ptr=base)
+    assert call(state=sb) == 1 and "intermediate_states: dtype f32, expected bf16" in detail(lib)
+    assert call(state=tens((Bn, H, P, N), I32, ptr=base)) == 1 and "dtype" in detail(lib)
     assert call(inter=tens((Bn, T + 1, H, P, N), F32, ptr=inter.data)) == 1
     assert call(inter=tens((Bn, T, H, P, N), F32, ptr=inter.data + 4)) == 3
     assert call(inter=tens((Bn, T, H, P, N), F32, ptr=base)) == 1 and "overlaps" in detail(lib)
@@ -337,6 +342,10 @@ def test_state_update_tokens_error_paths(lib):
     assert call(x=e((Bn, 0, H, P), BF16, x), dt=e((Bn, 0, H), F32, dt),
                 Bm=e((Bn, 0, G, N), BF16, Bm), Cm=e((Bn, 0, G, N), BF16, Cm),
                 out=e((Bn, 0, H, P), BF16, out), inter=e((Bn, 0, H, P, N), F32, inter),
+                parent=e((Bn, 0), I32, parent)) == 0
+    assert call(state=sb, x=e((Bn, 0, H, P), BF16, x), dt=e((Bn, 0, H), F32, dt),
+                Bm=e((Bn, 0, G, N), BF16, Bm), Cm=e((Bn, 0, G, N), BF16, Cm),
+                out=e((Bn, 0, H, P), BF16, out), inter=e((Bn, 0, H, P, N), BF16, inter),
                 parent=e((Bn, 0), I32, parent)) == 0
 
 

@@ -317,3 +317,40 @@ def test_tokens_pins_reject_planted_mistakes(mistake):
     for par in (None, parent):
         for a, b in zip(clean(**inp, parent=par), orc.ssu_tokens(**inp, parent=par)):
             np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-13)
+
+
+# ---- a state kept in bf16 (the pages' fp16 / bf16 state caches) -------------
+
+def test_bf16_state_rounds_only_what_is_kept():
+    inp = rand_token_inputs(seed=12)
+    # a kept state is bf16: start from bf16-representable values
+    inp["state"] = inp["state"].to(torch.bfloat16).to(f64)
+    out1, fin1, cache1 = orc.ssu_tokens(**{**inp, "x": inp["x"][:, :1], "dt": inp["dt"][:, :1],
+                                           "Bm": inp["Bm"][:, :1], "Cm": inp["Cm"][:, :1]},
+                                        state_dtype="bf16")
+    out0, fin0, _ = orc.ssu_tokens(**{**inp, "x": inp["x"][:, :1], "dt": inp["dt"][:, :1],
+                                      "Bm": inp["Bm"][:, :1], "Cm": inp["Cm"][:, :1]})
+    # one token: the output comes from the unrounded update; the kept state is
+    # that update rounded to bf16, nothing else changes
+    np.testing.assert_array_equal(out1, out0)
+    np.testing.assert_array_equal(fin1, torch.from_numpy(fin0).to(torch.bfloat16).to(f64).numpy())
+    np.testing.assert_array_equal(cache1[:, 0], fin1)
+    assert not np.array_equal(fin1, fin0)
+
+
+def test_bf16_state_tokens_equal_rounded_single_steps():
+    inp = rand_token_inputs(seed=13)
+    inp["state"] = inp["state"].to(torch.bfloat16).to(f64)
+    out, fin, cache = orc.ssu_tokens(**inp, state_dtype="bf16")
+    st = inp["state"]
+    T = inp["x"].shape[1]
+    for t in range(T):
+        o, new = orc.ssu_step(st, inp["x"][:, t], inp["dt"][:, t], inp["A"], inp["Bm"][:, t],
+                              inp["Cm"][:, t], D=inp["D"], ngroups=inp["ngroups"])
+        np.testing.assert_array_equal(out[:, t], o)
+        st = torch.from_numpy(new).to(torch.bfloat16).to(f64)
+        np.testing.assert_array_equal(cache[:, t], st.numpy())
+    np.testing.assert_array_equal(fin, st.numpy())
+    # and it stays within bf16 rounding of the float64 run
+    out64, fin64, _ = orc.ssu_tokens(**inp)
+    assert np.max(np.abs(out - out64)) / np.max(np.abs(out64)) < 2e-2

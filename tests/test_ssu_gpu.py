@@ -5,6 +5,13 @@ as max|gpu - ref| / max|ref|; the fp32 state within 1e-4 in both cases (it is
 computed in fp32 from the stored inputs, so only fp32 rounding separates it
 from the oracle).  Also: prefill with ssd_chunked_fwd followed by decode steps
 continues the same recurrence, and repeated calls are bitwise identical.
+
+A bf16 state is checked against the oracle's model of a bf16-kept state (the
+update from the stored values in float64, rounded to nearest even when kept):
+the kernel's fp32 update can land on the other side of a rounding boundary,
+so a kept element equals the oracle's or is one bf16 step (2^-7 of its
+magnitude at most, plus fp32 rounding where the update cancels) away, and
+almost all are equal.
 """
 import math
 
@@ -57,6 +64,7 @@ CASES = [
     (1, 128, 64, 128, 8, torch.bfloat16, True, True, False, False),
     (5, 3, 32, 64, 3, torch.float32, True, False, True, False),
     (4, 6, 128, 32, 2, torch.bfloat16, False, True, True, True),
+    (40, 16, 32, 128, 2, torch.float32, True, True, True, True),     # many 16 KB heads
 ]
 
 
@@ -154,6 +162,7 @@ TOKEN_CASES = [
     (1, 5, 4, 128, 128, 1, torch.float32, True, True, True),        # few heads: rows split
     (2, 3, 4, 16, 16, 2, torch.bfloat16, True, True, False),        # P below a pass of rows
     (5, 1, 3, 128, 32, 1, torch.float32, True, False, True),
+    (48, 3, 16, 64, 64, 4, torch.bfloat16, True, True, True),       # many 16 KB heads
 ]
 
 
@@ -208,3 +217,113 @@ def test_state_update_tokens_zero_tokens_is_a_no_op(ssd):
                                   dt_softplus=True, ngroups=2)
     torch.cuda.synchronize()
     assert out.shape == (2, 0, 4, 64) and torch.equal(state, dev["state"])
+
+
+# ---- a state kept in bf16 ----------------------------------------------------
+
+def bf16_step_check(got, ref, min_equal):
+    """got within one bf16 step of ref everywhere, and equal on at least
+    min_equal of the elements.  Where the update cancels (decayed state and
+    input term nearly opposite) the kept value is small and its bf16 step
+    smaller than the fp32 rounding of the two terms: 1e-5 max|ref| of slack
+    covers that (the terms are at most a few times max|ref|, fp32 keeps 2^-24
+    of them)."""
+    d = np.abs(got - ref)
+    assert np.all(d <= np.abs(ref) * 2.0 ** -7 + 1e-5 * np.max(np.abs(ref)))
+    assert np.mean(d == 0) >= min_equal
+
+
+BF16_STATE_CASES = [
+    # (B, H, P, N, G, dtype, z, bias, softplus)
+    (3, 8, 64, 128, 2, torch.bfloat16, True, True, True),
+    (2, 4, 16, 16, 1, torch.float32, False, False, False),
+    (64, 32, 64, 128, 8, torch.bfloat16, True, False, False),   # a full grid
+    (1, 6, 128, 32, 2, torch.float32, True, True, True),       # few heads: rows split
+]
+
+
+@pytest.mark.parametrize("case", BF16_STATE_CASES, ids=lambda c: f"B{c[0]}H{c[1]}P{c[2]}N{c[3]}"
+                         f"G{c[4]}-{str(c[5])[6:]}")
+def test_bf16_state_update_matches_oracle(ssd, case):
+    B, H, P, N, G, dtype, z, bias, sp = case
+    inp = make_step(B, H, P, N, G, dtype, seed=B * 31 + N, z=z, bias=bias, softplus=sp)
+    inp["state"] = inp["state"].to(torch.bfloat16)
+    u = lambda t: None if t is None else t.unsqueeze(1)
+    out_ref, fin_ref, _ = orc.ssu_tokens(**{**inp, "x": u(inp["x"]), "dt": u(inp["dt"]),
+                                            "Bm": u(inp["Bm"]), "Cm": u(inp["Cm"]),
+                                            "z": u(inp["z"])}, state_dtype="bf16")
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    state = dev.pop("state").clone()
+    out = ssd.state_update(state, dev["x"], dev["dt"], dev["A"], dev["Bm"], dev["Cm"],
+                           D=dev["D"], z=dev["z"], dt_bias=dev["dt_bias"],
+                           dt_softplus=dev["dt_softplus"], ngroups=G)
+    torch.cuda.synchronize()
+    assert state.dtype == torch.bfloat16
+    # out comes from the unrounded fp32 update: the fp32 bar when out is fp32
+    bar = 2e-2 if dtype == torch.bfloat16 else 1e-4
+    assert rel(out.double().cpu().numpy(), out_ref[:, 0]) <= bar
+    bf16_step_check(state.double().cpu().numpy(), fin_ref, 0.99)
+
+
+BF16_TOKEN_CASES = [
+    # (B, T, H, P, N, G, dtype, cache, tree, update)
+    (4, 4, 16, 64, 128, 2, torch.bfloat16, True, True, True),
+    (3, 6, 8, 64, 128, 8, torch.float32, True, False, True),
+    (2, 3, 4, 16, 16, 2, torch.bfloat16, True, True, False),
+    (32, 2, 32, 64, 128, 8, torch.bfloat16, False, False, True),    # a full grid
+    (40, 3, 16, 64, 128, 2, torch.bfloat16, True, True, True),      # a full grid, cache, tree
+    (40, 2, 16, 32, 64, 2, torch.float32, True, True, False),       # small heads
+]
+
+
+@pytest.mark.parametrize("case", BF16_TOKEN_CASES, ids=lambda c: f"B{c[0]}T{c[1]}H{c[2]}P{c[3]}"
+                         f"N{c[4]}G{c[5]}-{str(c[6])[6:]}-cache{int(c[7])}tree{int(c[8])}"
+                         f"up{int(c[9])}")
+def test_bf16_state_tokens_match_oracle(ssd, case):
+    B, T, H, P, N, G, dtype, cache, tree, update = case
+    inp = make_tokens(B, T, H, P, N, G, dtype, seed=B * 7 + T)
+    inp["state"] = inp["state"].to(torch.bfloat16)
+    parent = random_tree(B, T, seed=T + 1) if tree else None
+    out_ref, fin_ref, cache_ref = orc.ssu_tokens(**inp, parent=parent, update_state=update,
+                                                 state_dtype="bf16")
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    state = dev.pop("state").clone()
+    inter = torch.empty((B, T, H, P, N), dtype=torch.bfloat16, device="cuda") if cache else None
+    out = ssd.state_update_tokens(state, dev["x"], dev["dt"], dev["A"], dev["Bm"], dev["Cm"],
+                                  D=dev["D"], z=dev["z"], dt_bias=dev["dt_bias"],
+                                  dt_softplus=dev["dt_softplus"], ngroups=G,
+                                  intermediate_states=inter,
+                                  parent=None if parent is None else parent.cuda(),
+                                  update_state=update)
+    torch.cuda.synchronize()
+    # a rounding that went the other way at one token moves the later ones by
+    # about one bf16 step of that element: bars in units of max|ref|
+    bar = 2e-2 if dtype == torch.bfloat16 else 2e-3
+    assert rel(out.double().cpu().numpy(), out_ref) <= bar
+    if update:
+        assert rel(state.double().cpu().numpy(), fin_ref) <= 1e-2
+        assert np.mean(state.double().cpu().numpy() == fin_ref) >= 0.95
+    else:
+        assert torch.equal(state.cpu(), inp["state"])
+    if cache:
+        got = inter.double().cpu().numpy()
+        bf16_step_check(got[:, 0], cache_ref[:, 0], 0.99)   # the first token: one rounding
+        assert rel(got, cache_ref) <= 1e-2
+        assert np.mean(got == cache_ref) >= 0.95
+
+
+@pytest.mark.parametrize("B", [8, 64])
+def test_bf16_state_is_the_f32_update_rounded(ssd, B):
+    """One token: the bf16 state's update equals the f32 state's update (same
+    inputs, the state's values bf16) rounded to nearest even, bit for bit, and
+    the outputs are identical."""
+    inp = make_step(B, 16, 64, 128, 4, torch.bfloat16, seed=5, z=True, bias=True, softplus=True)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    sb = dev["state"].to(torch.bfloat16)
+    sf = sb.float()
+    kw = dict(D=dev["D"], z=dev["z"], dt_bias=dev["dt_bias"], dt_softplus=True, ngroups=4)
+    ob = ssd.state_update(sb, dev["x"], dev["dt"], dev["A"], dev["Bm"], dev["Cm"], **kw)
+    of = ssd.state_update(sf, dev["x"], dev["dt"], dev["A"], dev["Bm"], dev["Cm"], **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(ob, of)
+    assert torch.equal(sb, sf.to(torch.bfloat16))
