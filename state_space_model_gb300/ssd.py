@@ -134,8 +134,9 @@ def chunked_fwd_static_scratch(x, dt, A, B, C, D=None, initial_states=None, chun
 
 def state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
                  ngroups=1, *, out=None):
-    """One decode token (``ssd_state_update``): updates the fp32 ``state``
-    [B,H,P,N] in place and returns ``out`` [B,H,P] (dtype of x).  x, z
+    """One decode token (``ssd_state_update``): updates ``state`` [B,H,P,N]
+    (fp32, or bf16: computed in fp32, kept rounded) in place and returns
+    ``out`` [B,H,P] (dtype of x).  x, z
     [B,H,P]; dt [B,H]; A, D, dt_bias [H]; B, C [B,G,N]."""
     dev = _device_of(state, x, dt, A, B, C, D, z, dt_bias, out)
     if out is None:
@@ -154,7 +155,8 @@ def state_update_tokens(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_
                         out=None):
     """T decode tokens per sequence (``ssd_state_update_tokens``): x, z, out
     [B,T,H,P]; dt [B,T,H]; B, C [B,T,G,N]; optional intermediate_states
-    [B,T,H,P,N] f32 (the state after every token) and parent [B,T] int32
+    [B,T,H,P,N] in the state's dtype (the state after every token) and parent
+    [B,T] int32
     (token t starts from the state after token parent[b,t] when that is an
     earlier token).  Updates ``state`` in place unless ``update_state`` is
     false; returns ``out``."""
