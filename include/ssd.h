@@ -64,7 +64,7 @@ typedef enum {
     SSD_ERR_TIMEOUT = 6      /* a device-side bounded wait gave up           */
 } ssd_status;
 
-/* SSD_I32 only for the parent indices of ssd_state_update_tokens. */
+/* SSD_I32 only for the parent and state-slot indices of ssd_state_update_tokens. */
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1, SSD_I32 = 2 } ssd_dtype;
 
 typedef struct {
@@ -247,15 +247,25 @@ ssd_status ssd_state_update(ssd_tensor *state, const ssd_tensor *x, const ssd_te
  * as it was (a verification pass: the accepted step's intermediate state is
  * promoted by the caller).
  *
+ * Continuous batching (the serving kernel's state_batch_idx and pad_slot_id,
+ * same section): with state_indices given, the state and intermediate_states
+ * are pools of S slots and row b uses slot state_indices[b] of both (the
+ * state[b, h] and intermediate_states[b, t, h] above read [state_indices[b],
+ * ...]).  A row whose index lies outside [0, S) (a negative pad id, say) is
+ * padding: nothing is read or written for it, its out rows included.  Slots
+ * of real rows must be distinct (not checked: two rows on one slot race).
+ *
  * Shapes, dtypes and layouts (the token axis second):
  *   state [B, H, P, N] f32 or bf16, packed (bf16: rounded as for ssd_state_update,
- *         after every token: the s of the next token is the rounded one)
+ *         after every token: the s of the next token is the rounded one);
+ *         [S, H, P, N] with state_indices
  *   x, z, out [B, T, H, P] bf16 or f32 (z optional, out the dtype of x)
  *   dt    [B, T, H] f32                          A, D, dt_bias [H] f32
  *   B, C  [B, T, G, N] dtype of x, same strides
  *   intermediate_states [B, T, H, P, N] dtype of the state, packed, optional
- *         (required with parent)
+ *         (required with parent); [S, T, H, P, N] with state_indices
  *   parent [B, T] SSD_I32, optional
+ *   state_indices [B] SSD_I32, contiguous, optional
  * T = 1 without intermediate states or parents is ssd_state_update.  Alignment
  * as for ssd_state_update, plus intermediate_states 16-byte aligned.  Aliasing:
  * out, the state and intermediate_states overlap neither each other nor any
@@ -267,7 +277,8 @@ ssd_status ssd_state_update_tokens(ssd_tensor *state, const ssd_tensor *x, const
                                    const ssd_tensor *dt_bias, int32_t dt_softplus,
                                    int64_t ngroups, ssd_tensor *out,
                                    ssd_tensor *intermediate_states, const ssd_tensor *parent,
-                                   int32_t update_state, void *stream);
+                                   const ssd_tensor *state_indices, int32_t update_state,
+                                   void *stream);
 
 /* ---- mixer prologue ----------------------------------------------------------
  * The steps of the Mamba-2 mixer between its input projection and the scan, in

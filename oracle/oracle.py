@@ -333,7 +333,7 @@ def _round_state(a, state_dtype):
 
 
 def ssu_tokens(state, x, dt, A, Bm, Cm, D=None, z=None, dt_bias=None, dt_softplus=False,
-               ngroups=1, parent=None, update_state=True, state_dtype=None):
+               ngroups=1, parent=None, update_state=True, state_dtype=None, state_indices=None):
     """T decode steps per sequence, in float64, as one would apply them one
     token at a time -- the multi-token state update of "Optimizing Nemotron
     v3 Super in TensorRT-LLM", section 10.4, with the intermediate-state cache
@@ -352,6 +352,13 @@ def ssu_tokens(state, x, dt, A, Bm, Cm, D=None, z=None, dt_bias=None, dt_softplu
     token's update is computed from the kept state in float64 and its output
     from the unrounded result, and the state is then kept rounded (the running
     state, the cache and the final state alike).  None keeps float64 throughout.
+
+    ``state_indices`` [B] integers (the slot indirection of the page's serving
+    kernel, section 10.4: state_batch_idx, with pad_slot_id for padding rows)
+    makes ``state`` a pool [S,H,P,N] of S slots: sequence b runs on
+    state[state_indices[b]], and a row whose index is outside [0, S) is padding:
+    it is not computed (its out and cache rows are NaN) and no slot changes for
+    it.  ``final`` is then the whole pool, the slots of real rows updated.
     """
     f = lambda t: None if t is None else _as_cpu(t).to(torch.float64)
     st0 = f(state)
@@ -360,11 +367,16 @@ def ssu_tokens(state, x, dt, A, Bm, Cm, D=None, z=None, dt_bias=None, dt_softplu
     H, P, N = st0.shape[1], st0.shape[2], st0.shape[3]
     par = None if parent is None else np.asarray(torch.as_tensor(parent).detach().cpu().numpy(),
                                                  dtype=np.int64)
-    out = np.empty((Bn, T, H, P), dtype=np.float64)
-    cache = np.empty((Bn, T, H, P, N), dtype=np.float64)
+    slots = np.arange(Bn) if state_indices is None else np.asarray(
+        torch.as_tensor(state_indices).detach().cpu().numpy(), dtype=np.int64)
+    out = np.full((Bn, T, H, P), np.nan, dtype=np.float64)
+    cache = np.full((Bn, T, H, P, N), np.nan, dtype=np.float64)
     final = st0.numpy().copy()
     for b in range(Bn):
-        run = st0[b:b + 1]
+        slot = int(slots[b])
+        if not 0 <= slot < st0.shape[0]:
+            continue                                    # a padding row
+        run = st0[slot:slot + 1]
         for t in range(T):
             if par is not None and t > 0 and 0 <= par[b, t] < t:
                 run = torch.from_numpy(cache[b:b + 1, par[b, t]].copy())
@@ -377,7 +389,7 @@ def ssu_tokens(state, x, dt, A, Bm, Cm, D=None, z=None, dt_bias=None, dt_softplu
             cache[b, t] = new[0]
             run = torch.from_numpy(new)
         if update_state and T > 0:
-            final[b] = run[0].numpy()
+            final[slot] = run[0].numpy()
     return out, final, cache
 
 

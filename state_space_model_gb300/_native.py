@@ -48,8 +48,8 @@ SIGNATURES = {
     "ssd_device_status": [_VP],
     "ssd_selftest_wait_timeout": [ctypes.c_uint64, _VP],
     "ssd_state_update": [_T, _T, _T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _VP],
-    "ssd_state_update_tokens": [_T, _T, _T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _T, _T, _I32,
-                                _VP],
+    "ssd_state_update_tokens": [_T, _T, _T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _T, _T, _T,
+                                _I32, _VP],
     "ssd_mixer_prologue": [_T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _T, _T, _T, _VP],
     "ssd_stage_chunk_cumsum": [_T, _T, _I64, _T, _VP],
     "ssd_stage_chunk_state": [_T, _T, _T, _T, _I64, _I64, _T, _VP],

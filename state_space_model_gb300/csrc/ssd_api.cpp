@@ -489,18 +489,26 @@ ssd_status state_update_impl(bool tokens, ssd_tensor *state, const ssd_tensor *x
                              const ssd_tensor *Cm, const ssd_tensor *D, const ssd_tensor *z,
                              const ssd_tensor *dt_bias, int32_t dt_softplus, int64_t ngroups,
                              ssd_tensor *out, ssd_tensor *inter, const ssd_tensor *parent,
-                             int32_t update_state, void *stream) {
+                             const ssd_tensor *slots, int32_t update_state, void *stream) {
     if (!state) return fail(SSD_ERR_INVALID_ARG, "state: null tensor descriptor");
     if (state->ndim != 4) return fail(SSD_ERR_INVALID_ARG, "state: ndim %d, expected 4",
                                       state->ndim);
     if (!x) return fail(SSD_ERR_INVALID_ARG, "x: null tensor descriptor");
     if (tokens && x->ndim != 4)
         return fail(SSD_ERR_INVALID_ARG, "x: ndim %d, expected 4", x->ndim);
-    const int64_t Bn = state->shape[0], H = state->shape[1], P = state->shape[2],
-                  N = state->shape[3], G = ngroups, T = tokens ? x->shape[1] : 1;
-    if (Bn < 0 || T < 0)
-        return fail(SSD_ERR_INVALID_ARG, "batch %lld / tokens %lld negative", (long long)Bn,
-                    (long long)T);
+    // rows come from x; the state holds one entry per row, or a pool of S
+    // slots addressed through `slots`
+    const int64_t Bn = x->shape[0], S = state->shape[0], H = state->shape[1],
+                  P = state->shape[2], N = state->shape[3], G = ngroups,
+                  T = tokens ? x->shape[1] : 1;
+    if (Bn < 0 || T < 0 || S < 0)
+        return fail(SSD_ERR_INVALID_ARG, "batch %lld / tokens %lld / state slots %lld negative",
+                    (long long)Bn, (long long)T, (long long)S);
+    if (!slots && S != Bn)
+        return fail(SSD_ERR_INVALID_ARG, "state: shape[0] = %lld, expected the batch %lld (or "
+                    "give state_indices)", (long long)S, (long long)Bn);
+    if (slots && S > (int64_t(1) << 31) - 1)
+        return fail(SSD_ERR_UNSUPPORTED, "state pool of %lld slots above 2^31 - 1", (long long)S);
     if (H <= 0 || G <= 0) return fail(SSD_ERR_INVALID_ARG, "nheads %lld / ngroups %lld must be "
                                       "positive", (long long)H, (long long)G);
     if (H % G) return fail(SSD_ERR_INVALID_ARG, "nheads %lld is not a multiple of ngroups %lld",
@@ -520,11 +528,11 @@ ssd_status state_update_impl(bool tokens, ssd_tensor *state, const ssd_tensor *x
     const int xdt = x->dtype;
     // shapes with the token axis (index 1) when `tokens`, without it otherwise
     const int k = tokens ? 1 : 0;
-    const int64_t sst[4] = {Bn, H, P, N};
+    const int64_t sst[4] = {S, H, P, N};
     const int64_t sx4[4] = {Bn, T, H, P}, sx3[3] = {Bn, H, P};
     const int64_t sdt3[3] = {Bn, T, H}, sdt2[2] = {Bn, H};
     const int64_t sbc4[4] = {Bn, T, G, N}, sbc3[3] = {Bn, G, N};
-    const int64_t sh[1] = {H}, sin[5] = {Bn, T, H, P, N}, spar[2] = {Bn, T};
+    const int64_t sh[1] = {H}, sin[5] = {S, T, H, P, N}, spar[2] = {Bn, T}, sslot[1] = {Bn};
     const int64_t *sx = tokens ? sx4 : sx3, *sdt = tokens ? sdt3 : sdt2,
                   *sbc = tokens ? sbc4 : sbc3;
     ssd_status st;
@@ -547,12 +555,16 @@ ssd_status state_update_impl(bool tokens, ssd_tensor *state, const ssd_tensor *x
         return st;
     if (parent && (st = check_tensor(parent, "parent", 2, spar, SSD_I32, false, false)))
         return st;
+    if (slots && (st = check_tensor(slots, "state_indices", 1, sslot, SSD_I32, true, false)))
+        return st;
 
-    const Range ins[] = {range_of(x), range_of(dt), range_of(A), range_of(Bm), range_of(Cm),
-                         range_of(D), range_of(z), range_of(dt_bias), range_of(parent)};
-    const char *in_names[] = {"x", "dt", "A", "B", "C", "D", "z", "dt_bias", "parent"};
+    const Range ins[] = {range_of(x),  range_of(dt), range_of(A),       range_of(Bm),
+                         range_of(Cm), range_of(D),  range_of(z),       range_of(dt_bias),
+                         range_of(parent), range_of(slots)};
+    const char *in_names[] = {"x", "dt", "A", "B", "C", "D", "z", "dt_bias", "parent",
+                              "state_indices"};
     const Range rs = range_of(state), ro = range_of(out), ri = range_of(inter);
-    for (int i = 0; i < 9; ++i) {
+    for (int i = 0; i < 10; ++i) {
         if (overlap(ro, ins[i])) return fail(SSD_ERR_INVALID_ARG, "out overlaps %s", in_names[i]);
         if (overlap(rs, ins[i]))
             return fail(SSD_ERR_INVALID_ARG, "state overlaps %s", in_names[i]);
@@ -567,7 +579,8 @@ ssd_status state_update_impl(bool tokens, ssd_tensor *state, const ssd_tensor *x
     if ((st = check_device_ptrs({{dp(state), "state"}, {dp(x), "x"}, {dp(dt), "dt"},
                                  {dp(A), "A"}, {dp(Bm), "B"}, {dp(Cm), "C"}, {dp(D), "D"},
                                  {dp(z), "z"}, {dp(dt_bias), "dt_bias"}, {dp(out), "out"},
-                                 {dp(inter), "intermediate_states"}, {dp(parent), "parent"}})))
+                                 {dp(inter), "intermediate_states"}, {dp(parent), "parent"},
+                                 {dp(slots), "state_indices"}})))
         return st;
 
     // stride of the token axis (0 without one) and of the axes after it
@@ -611,6 +624,8 @@ ssd_status state_update_impl(bool tokens, ssd_tensor *state, const ssd_tensor *x
     a.inter = inter ? inter->data : nullptr;
     a.parent = parent ? static_cast<const int32_t *>(parent->data) : nullptr;
     a.par_sb = parent ? parent->stride[0] : 0;
+    a.slots = slots ? static_cast<const int32_t *>(slots->data) : nullptr;
+    a.S = int(S);
     return cuda_status(ssd::launch_ssu(a, static_cast<cudaStream_t>(stream)), "state update");
 }
 
@@ -621,7 +636,7 @@ ssd_status ssd_state_update(ssd_tensor *state, const ssd_tensor *x, const ssd_te
                             const ssd_tensor *D, const ssd_tensor *z, const ssd_tensor *dt_bias,
                             int32_t dt_softplus, int64_t ngroups, ssd_tensor *out, void *stream) {
     return state_update_impl(false, state, x, dt, A, Bm, Cm, D, z, dt_bias, dt_softplus, ngroups,
-                             out, nullptr, nullptr, 1, stream);
+                             out, nullptr, nullptr, nullptr, 1, stream);
 }
 
 ssd_status ssd_state_update_tokens(ssd_tensor *state, const ssd_tensor *x, const ssd_tensor *dt,
@@ -630,9 +645,11 @@ ssd_status ssd_state_update_tokens(ssd_tensor *state, const ssd_tensor *x, const
                                    const ssd_tensor *dt_bias, int32_t dt_softplus,
                                    int64_t ngroups, ssd_tensor *out,
                                    ssd_tensor *intermediate_states, const ssd_tensor *parent,
-                                   int32_t update_state, void *stream) {
+                                   const ssd_tensor *state_indices, int32_t update_state,
+                                   void *stream) {
     return state_update_impl(true, state, x, dt, A, Bm, Cm, D, z, dt_bias, dt_softplus, ngroups,
-                             out, intermediate_states, parent, update_state, stream);
+                             out, intermediate_states, parent, state_indices, update_state,
+                             stream);
 }
 
 ssd_status ssd_mixer_prologue(const ssd_tensor *xBC, const ssd_tensor *conv_weight,

@@ -66,6 +66,8 @@ struct SsuArgs {
     void *inter = nullptr;                    // may be null (not cached)
     const int32_t *parent = nullptr;          // may be null (a chain)
     int64_t par_sb = 0;
+    const int32_t *slots = nullptr;           // may be null (row b uses state b)
+    int S = 0;                                // slots in the state pool
 };
 cudaError_t launch_ssu(const SsuArgs &a, cudaStream_t stream);
 

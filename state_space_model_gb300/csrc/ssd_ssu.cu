@@ -8,7 +8,10 @@
 //     out   = (state C + D x) * silu(z)
 // for every (batch, head), head h reading group h / (H / G); token t > 0 may
 // start from the cached state after an earlier token (its parent) instead of
-// the one after token t - 1.
+// the one after token t - 1.  With slot indices (the serving kernel's
+// state_batch_idx of section 10.4) sequence b's state and cache live in slot
+// slots[b] of a pool; a row whose slot is outside the pool is padding and is
+// skipped.
 //
 // The state is kept in fp32 or, as in section 6.4.3's Blackwell path for
 // 16-bit state caches, in bf16: each token's update is computed in fp32 from
@@ -121,11 +124,16 @@ k_ssu_tokens(const SsuArgs a, int rows, unsigned int *err) {
     __shared__ uint64_t full;
     __shared__ float xs[2][128], gs[2][128], ps[2][128];   // rows <= P <= 128
     const int b = blockIdx.z, h = blockIdx.y;
+    int64_t slot = b;                               // where row b's state and cache live
+    if (a.slots) {
+        slot = a.slots[b];
+        if (slot < 0 || slot >= a.S) return;        // a padding row: nothing read or written
+    }
     const int g = h / (a.H / a.G);
     const int r0 = blockIdx.x * rows;
     const int c = threadIdx.x % kTpr, rr = threadIdx.x / kTpr;
     const int nrt = (rows + kRowsPass - 1) / kRowsPass;   // uniform over the CTA
-    const size_t head = size_t(b) * a.H + h;
+    const size_t head = size_t(slot) * a.H + h;
     S *st = static_cast<S *>(a.state) + (head * a.P + r0) * N;
     const uint32_t bytes = uint32_t(rows) * N * uint32_t(sizeof(S));
 
@@ -195,7 +203,7 @@ k_ssu_tokens(const SsuArgs a, int rows, unsigned int *err) {
             const int pt = a.parent[int64_t(b) * a.par_sb + t];
             if (pt >= 0 && pt < t) {
                 const S *src = static_cast<const S *>(a.inter) +
-                               ((int64_t(b) * a.T + pt) * a.H + h) * a.P * N;
+                               ((slot * a.T + pt) * a.H + h) * a.P * N;
                 for (int i = 0; i < nrt; ++i) {
                     const int lr = rr + i * kRowsPass;
                     if (lr < rows)
@@ -211,7 +219,7 @@ k_ssu_tokens(const SsuArgs a, int rows, unsigned int *err) {
         if (t + 1 < a.T) stage_xz(t + 1);           // the other buffer, read after the next sync
         const float *xt = xs[t & 1];
         float *sums = ps[t & 1];
-        S *ir = a.inter ? static_cast<S *>(a.inter) + ((int64_t(b) * a.T + t) * a.H + h) * a.P * N
+        S *ir = a.inter ? static_cast<S *>(a.inter) + ((slot * a.T + t) * a.H + h) * a.P * N
                         : nullptr;
 #pragma unroll 4
         for (int i = 0; i < nrt; ++i) {

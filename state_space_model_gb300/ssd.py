@@ -152,15 +152,19 @@ def state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplu
 
 def state_update_tokens(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
                         ngroups=1, *, intermediate_states=None, parent=None, update_state=True,
-                        out=None):
+                        state_indices=None, out=None):
     """T decode tokens per sequence (``ssd_state_update_tokens``): x, z, out
     [B,T,H,P]; dt [B,T,H]; B, C [B,T,G,N]; optional intermediate_states
     [B,T,H,P,N] in the state's dtype (the state after every token) and parent
     [B,T] int32
     (token t starts from the state after token parent[b,t] when that is an
     earlier token).  Updates ``state`` in place unless ``update_state`` is
-    false; returns ``out``."""
-    dev = _device_of(state, x, dt, A, B, C, D, z, dt_bias, intermediate_states, parent, out)
+    false; returns ``out``.  ``state_indices`` [B] int32 makes ``state`` and
+    ``intermediate_states`` pools of S slots ([S,H,P,N], [S,T,H,P,N]): row b
+    uses slot state_indices[b]; rows with an index outside [0, S) are skipped
+    (their out rows are not written)."""
+    dev = _device_of(state, x, dt, A, B, C, D, z, dt_bias, intermediate_states, parent,
+                     state_indices, out)
     if out is None:
         out = torch.empty(x.shape, dtype=x.dtype, device=dev)
     lib = _native.load()
@@ -168,7 +172,8 @@ def state_update_tokens(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_
                                               _desc(B), _desc(C), _desc(D), _desc(z),
                                               _desc(dt_bias), 1 if dt_softplus else 0, ngroups,
                                               _desc(out), _desc(intermediate_states),
-                                              _desc(parent), 1 if update_state else 0,
+                                              _desc(parent), _desc(state_indices),
+                                              1 if update_state else 0,
                                               _stream(dev)),
                   "ssd_state_update_tokens")
     return out

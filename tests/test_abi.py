@@ -315,13 +315,13 @@ def test_state_update_tokens_error_paths(lib):
 
     def call(**kw):
         a = dict(state=state, x=x, dt=dt, A=A, Bm=Bm, Cm=Cm, out=out, inter=inter, parent=parent,
-                 upd=1)
+                 slots=None, upd=1)
         a.update(kw)
         q = lambda t: None if t is None else p(t)
         return lib.ssd_state_update_tokens(q(a["state"]), q(a["x"]), q(a["dt"]), q(a["A"]),
                                            q(a["Bm"]), q(a["Cm"]), None, None, None, 0, G,
-                                           q(a["out"]), q(a["inter"]), q(a["parent"]), a["upd"],
-                                           None)
+                                           q(a["out"]), q(a["inter"]), q(a["parent"]),
+                                           q(a["slots"]), a["upd"], None)
 
     assert call(inter=None) == 1 and "parent needs intermediate_states" in detail(lib)
     assert call(parent=tens((Bn, T), F32, ptr=parent.data)) == 1 and "dtype" in detail(lib)
@@ -337,11 +337,28 @@ def test_state_update_tokens_error_paths(lib):
     assert call(inter=tens((Bn, T, H, P, N), F32, ptr=base)) == 1 and "overlaps" in detail(lib)
     # int32 is accepted only where it is asked for
     assert call(x=tens((Bn, T, H, P), I32, ptr=x.data)) == 1 and "dtype" in detail(lib)
+    # a state pool of S slots needs state_indices [B] int32, the cache a pool too
+    S = 5
+    pool = tens((S, H, P, N), F32, ptr=base + (9 << 24))
+    ipool = tens((S, T, H, P, N), F32, ptr=base + (10 << 24))
+    slots = tens((Bn,), I32, ptr=base + (11 << 24))
+    assert call(state=pool) == 1 and "state_indices" in detail(lib)
+    assert call(state=pool, slots=slots) == 1 and "intermediate_states: shape[0]" in detail(lib)
+    assert call(state=pool, inter=ipool, slots=tens((Bn,), F32, ptr=slots.data)) == 1 and \
+        "state_indices: dtype" in detail(lib)
+    assert call(state=pool, inter=ipool, slots=tens((Bn + 1,), I32, ptr=slots.data)) == 1 and \
+        "state_indices: shape" in detail(lib)
+    assert call(state=pool, inter=ipool, slots=tens((Bn,), I32, ptr=pool.data)) == 1 and \
+        "overlaps" in detail(lib)
     # no parent and no cache is valid as far as the host checks go; T = 0 launches nothing
     e = lambda shape, dtype, t: tens(shape, dtype, ptr=t.data)
     assert call(x=e((Bn, 0, H, P), BF16, x), dt=e((Bn, 0, H), F32, dt),
                 Bm=e((Bn, 0, G, N), BF16, Bm), Cm=e((Bn, 0, G, N), BF16, Cm),
                 out=e((Bn, 0, H, P), BF16, out), inter=e((Bn, 0, H, P, N), F32, inter),
+                parent=e((Bn, 0), I32, parent)) == 0
+    assert call(state=pool, slots=slots, x=e((Bn, 0, H, P), BF16, x), dt=e((Bn, 0, H), F32, dt),
+                Bm=e((Bn, 0, G, N), BF16, Bm), Cm=e((Bn, 0, G, N), BF16, Cm),
+                out=e((Bn, 0, H, P), BF16, out), inter=e((S, 0, H, P, N), F32, inter),
                 parent=e((Bn, 0), I32, parent)) == 0
     assert call(state=sb, x=e((Bn, 0, H, P), BF16, x), dt=e((Bn, 0, H), F32, dt),
                 Bm=e((Bn, 0, G, N), BF16, Bm), Cm=e((Bn, 0, G, N), BF16, Cm),

@@ -354,3 +354,38 @@ def test_bf16_state_tokens_equal_rounded_single_steps():
     # and it stays within bf16 rounding of the float64 run
     out64, fin64, _ = orc.ssu_tokens(**inp)
     assert np.max(np.abs(out - out64)) / np.max(np.abs(out64)) < 2e-2
+
+
+# ---- slot indirection (a state pool and padding rows) ------------------------
+
+@pytest.mark.parametrize("indices", [[3, -1, 0], [4, 7, 1]], ids=["pad_negative", "pad_past_end"])
+def test_slots_run_each_row_on_its_slot(indices):
+    B, S = 3, 5
+    inp = rand_token_inputs(B=B, seed=14)
+    g = torch.Generator().manual_seed(15)
+    pool = 0.3 * torch.randn((S,) + tuple(inp["state"].shape[1:]), generator=g, dtype=f64)
+    idx = torch.tensor(indices, dtype=torch.int32)
+    out, final, cache = orc.ssu_tokens(**{**inp, "state": pool}, state_indices=idx)
+    used = set()
+    for b, slot in enumerate(indices):
+        if not 0 <= slot < S:               # padding: nothing computed for the row
+            assert np.all(np.isnan(out[b])) and np.all(np.isnan(cache[b]))
+            continue
+        used.add(slot)
+        # the C recurrence of row b's tokens from the slot's state
+        y, fin = orc.recurrence(inp["x"][b:b + 1], inp["dt"][b:b + 1], inp["A"],
+                                inp["Bm"][b:b + 1], inp["Cm"][b:b + 1], inp["D"],
+                                pool[slot:slot + 1], ngroups=inp["ngroups"])
+        np.testing.assert_allclose(out[b], y[0], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(final[slot], fin[0], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(cache[b, -1], fin[0], rtol=1e-12, atol=1e-12)
+    for slot in set(range(S)) - used:       # other slots untouched, bit for bit
+        np.testing.assert_array_equal(final[slot], pool[slot].numpy())
+
+
+def test_identity_slots_equal_the_plain_call():
+    inp = rand_token_inputs(seed=16)
+    a = orc.ssu_tokens(**inp)
+    b = orc.ssu_tokens(**inp, state_indices=torch.arange(inp["x"].shape[0], dtype=torch.int32))
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u, v)

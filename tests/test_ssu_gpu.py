@@ -327,3 +327,59 @@ def test_bf16_state_is_the_f32_update_rounded(ssd, B):
     torch.cuda.synchronize()
     assert torch.equal(ob, of)
     assert torch.equal(sb, sf.to(torch.bfloat16))
+
+
+# ---- slot indirection: a state pool and padding rows --------------------------
+
+SLOT_CASES = [
+    # (B, S, T, H, P, N, G, dtype, state dtype, cache, tree)
+    (6, 9, 3, 8, 64, 128, 2, torch.bfloat16, torch.float32, True, True),
+    (5, 7, 1, 4, 32, 64, 1, torch.float32, torch.bfloat16, True, False),
+    (64, 80, 2, 32, 64, 128, 8, torch.bfloat16, torch.float32, False, False),   # a full grid
+]
+
+
+@pytest.mark.parametrize("case", SLOT_CASES, ids=lambda c: f"B{c[0]}S{c[1]}T{c[2]}H{c[3]}P{c[4]}"
+                         f"N{c[5]}-{str(c[7])[6:]}-state{str(c[8])[6:]}-cache{int(c[9])}"
+                         f"tree{int(c[10])}")
+def test_state_slots_match_oracle(ssd, case):
+    B, S, T, H, P, N, G, dtype, sdt, cache, tree = case
+    inp = make_tokens(B, T, H, P, N, G, dtype, seed=B + S + T)
+    g = torch.Generator().manual_seed(S)
+    pool = (0.5 * torch.randn((S, H, P, N), generator=g)).to(sdt)
+    idx = torch.randperm(S, generator=g)[:B].to(torch.int32)
+    idx[1], idx[-1] = -1, S + 3                 # two padding rows: a pad id and one past the pool
+    parent = random_tree(B, T, seed=T + 2) if tree else None
+    bf = sdt == torch.bfloat16
+    out_ref, fin_ref, cache_ref = orc.ssu_tokens(**{**inp, "state": pool}, parent=parent,
+                                                 state_dtype="bf16" if bf else None,
+                                                 state_indices=idx)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    state = pool.cuda()
+    inter = torch.full((S, T, H, P, N), 3.0, dtype=sdt, device="cuda") if cache else None
+    out = torch.full((B, T, H, P), 7.0, dtype=dtype, device="cuda")
+    ssd.state_update_tokens(state, dev["x"], dev["dt"], dev["A"], dev["Bm"], dev["Cm"],
+                            D=dev["D"], z=dev["z"], dt_bias=dev["dt_bias"],
+                            dt_softplus=dev["dt_softplus"], ngroups=G, intermediate_states=inter,
+                            parent=None if parent is None else parent.cuda(),
+                            state_indices=idx.cuda(), out=out)
+    torch.cuda.synchronize()
+    real = [b for b in range(B) if 0 <= int(idx[b]) < S]
+    used = [int(idx[b]) for b in real]
+    o = out.double().cpu().numpy()
+    bar = 2e-2 if dtype == torch.bfloat16 else (2e-3 if bf else 1e-4)
+    assert rel(o[real], out_ref[real]) <= bar
+    assert np.all(o[[1, B - 1]] == 7.0)         # padding rows: out not written
+    st = state.double().cpu().numpy()
+    if bf and T == 1:
+        bf16_step_check(st[used], fin_ref[used], 0.99)
+    elif bf:
+        assert rel(st[used], fin_ref[used]) <= 1e-2
+    else:
+        assert rel(st[used], fin_ref[used]) <= 1e-4
+    unused = sorted(set(range(S)) - set(used))
+    assert torch.equal(state[unused].cpu(), pool[unused])      # other slots untouched
+    if cache:
+        ic = inter.double().cpu().numpy()
+        assert rel(ic[used], cache_ref[real]) <= (1e-2 if bf else 1e-4)
+        assert np.all(ic[unused] == 3.0)
