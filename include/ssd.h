@@ -64,7 +64,8 @@ typedef enum {
     SSD_ERR_TIMEOUT = 6      /* a device-side bounded wait gave up           */
 } ssd_status;
 
-/* SSD_I32 only for the parent and state-slot indices of ssd_state_update_tokens. */
+/* SSD_I32 only for the parent and state-slot indices of ssd_state_update_tokens
+ * and the conv-state slot indices of ssd_mixer_prologue. */
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1, SSD_I32 = 2 } ssd_dtype;
 
 typedef struct {
@@ -304,6 +305,12 @@ ssd_status ssd_state_update_tokens(ssd_tensor *state, const ssd_tensor *x, const
  *     current token); conv_bias [Dc] f32, optional
  *   conv_state [B, Dc, W] dtype of xBC, packed, optional
  *   conv_windows [B, L, Dc, W] dtype of xBC, packed, optional
+ *   conv_state_indices [B] SSD_I32, contiguous, optional (needs conv_state):
+ *     the conv_state_indices of section 10.5 -- conv_state and conv_windows
+ *     become pools [S, Dc, W] and [S, L, Dc, W] and row b reads and writes
+ *     slot conv_state_indices[b] of both; a row whose index lies outside
+ *     [0, S) is padding: nothing is read or written for it, its x, B, C and
+ *     dt_out rows included.  Real rows must name distinct slots (not checked).
  *   dt, dt_out [B, L, H] f32; dt_bias [H] f32, optional
  *   x [B, L, H, P], B and C [B, L, G, N], dtype of xBC (outputs)
  * The outputs are what ssd_chunked_fwd takes as x, dt, B and C.  Alignment:
@@ -314,10 +321,10 @@ ssd_status ssd_state_update_tokens(ssd_tensor *state, const ssd_tensor *x, const
  * a sequence is split over several CTAs, which needs L > 8), no workspace. */
 ssd_status ssd_mixer_prologue(const ssd_tensor *xBC, const ssd_tensor *conv_weight,
                               const ssd_tensor *conv_bias, ssd_tensor *conv_state,
-                              ssd_tensor *conv_windows, const ssd_tensor *dt,
-                              const ssd_tensor *dt_bias, int32_t dt_softplus, int64_t ngroups,
-                              ssd_tensor *x, ssd_tensor *B, ssd_tensor *C, ssd_tensor *dt_out,
-                              void *stream);
+                              ssd_tensor *conv_windows, const ssd_tensor *conv_state_indices,
+                              const ssd_tensor *dt, const ssd_tensor *dt_bias,
+                              int32_t dt_softplus, int64_t ngroups, ssd_tensor *x,
+                              ssd_tensor *B, ssd_tensor *C, ssd_tensor *dt_out, void *stream);
 
 /* ---- stage entry points (the four steps of ssd_chunked_fwd, one call each;
  *      same conventions; used to check each step on its own) ---------------- */

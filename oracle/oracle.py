@@ -393,7 +393,7 @@ def ssu_tokens(state, x, dt, A, Bm, Cm, D=None, z=None, dt_bias=None, dt_softplu
     return out, final, cache
 
 
-def causal_conv1d(xBC, weight, bias=None, conv_state=None, silu=True):
+def causal_conv1d(xBC, weight, bias=None, conv_state=None, silu=True, state_indices=None):
     """Causal depthwise convolution over the token axis, then SiLU -- the
     convolution that prepares x, B and C in the Mamba-2 mixer ("Optimizing
     Nemotron v3 Super in TensorRT-LLM", sections 8 "CausalConv1d Optimization"
@@ -409,7 +409,24 @@ def causal_conv1d(xBC, weight, bias=None, conv_state=None, silu=True):
     ``(out [B, L, Dc], new_state [B, Dc, W], windows [B, L, Dc, W])``:
     new_state holds the last W inputs of the concatenation, windows[:, t] the
     last W inputs up to and including token t (the state after token t).
+
+    ``state_indices`` [B] integers (the conv_state_indices of the page's
+    section 10.5) makes ``conv_state`` a pool [S, Dc, W]: row b reads and
+    replaces slot state_indices[b]; a row whose index is outside [0, S) is
+    padding, not computed (its out and windows rows are NaN), and
+    ``new_state`` is the whole pool with the slots of real rows replaced.
     """
+    if state_indices is not None:
+        pool = _as_cpu(conv_state).to(torch.float64).numpy()
+        slots = np.asarray(torch.as_tensor(state_indices).cpu().numpy(), dtype=np.int64)
+        real = (slots >= 0) & (slots < pool.shape[0])
+        rows = np.where(real[:, None, None], pool[np.where(real, slots, 0)], 0.0)
+        out, new_rows, windows = causal_conv1d(xBC, weight, bias, torch.from_numpy(rows), silu)
+        out[~real] = np.nan
+        windows[~real] = np.nan
+        new_pool = pool.copy()
+        new_pool[slots[real]] = new_rows[real]
+        return out, new_pool, windows
     xv = _as_cpu(xBC).to(torch.float64).numpy()
     w = _as_cpu(weight).to(torch.float64).numpy()
     Bn, L, Dc = xv.shape

@@ -50,7 +50,7 @@ SIGNATURES = {
     "ssd_state_update": [_T, _T, _T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _VP],
     "ssd_state_update_tokens": [_T, _T, _T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _T, _T, _T,
                                 _I32, _VP],
-    "ssd_mixer_prologue": [_T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _T, _T, _T, _VP],
+    "ssd_mixer_prologue": [_T, _T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _T, _T, _T, _VP],
     "ssd_stage_chunk_cumsum": [_T, _T, _I64, _T, _VP],
     "ssd_stage_chunk_state": [_T, _T, _T, _T, _I64, _I64, _T, _VP],
     "ssd_stage_state_passing": [_T, _T, _T, _I64, _T, _T, _VP],

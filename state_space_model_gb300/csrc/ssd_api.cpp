@@ -654,7 +654,8 @@ ssd_status ssd_state_update_tokens(ssd_tensor *state, const ssd_tensor *x, const
 
 ssd_status ssd_mixer_prologue(const ssd_tensor *xBC, const ssd_tensor *conv_weight,
                               const ssd_tensor *conv_bias, ssd_tensor *conv_state,
-                              ssd_tensor *conv_windows, const ssd_tensor *dt,
+                              ssd_tensor *conv_windows, const ssd_tensor *conv_state_indices,
+                              const ssd_tensor *dt,
                               const ssd_tensor *dt_bias, int32_t dt_softplus, int64_t ngroups,
                               ssd_tensor *x, ssd_tensor *Bm, ssd_tensor *Cm, ssd_tensor *dt_out,
                               void *stream) {
@@ -684,9 +685,15 @@ ssd_status ssd_mixer_prologue(const ssd_tensor *xBC, const ssd_tensor *conv_weig
         return fail(SSD_ERR_UNSUPPORTED, "batch %lld above 65535 or seqlen %lld above 4194240",
                     (long long)Bn, (long long)L);
     const int xdt = xBC->dtype;
-    const int64_t sin[3] = {Bn, L, Dc}, sw[2] = {Dc, W}, sb[1] = {Dc}, sst[3] = {Bn, Dc, W},
-                  swin[4] = {Bn, L, Dc, W}, sdt[3] = {Bn, L, H}, sh[1] = {H},
-                  sx[4] = {Bn, L, H, P}, sbc[4] = {Bn, L, G, N};
+    // with slot indices the conv state and windows are pools of S slots
+    if (conv_state_indices && !conv_state)
+        return fail(SSD_ERR_INVALID_ARG, "conv_state_indices needs conv_state (the slot pool)");
+    const int64_t S = conv_state_indices ? conv_state->shape[0] : Bn;
+    if (S < 0 || S > (int64_t(1) << 31) - 1)
+        return fail(SSD_ERR_INVALID_ARG, "conv_state: %lld slots", (long long)S);
+    const int64_t sin[3] = {Bn, L, Dc}, sw[2] = {Dc, W}, sb[1] = {Dc}, sst[3] = {S, Dc, W},
+                  swin[4] = {S, L, Dc, W}, sdt[3] = {Bn, L, H}, sh[1] = {H},
+                  sx[4] = {Bn, L, H, P}, sbc[4] = {Bn, L, G, N}, sslot[1] = {Bn};
     ssd_status st;
     if ((st = check_tensor(xBC, "xBC", 3, sin, -1, false, true))) return st;
     if ((st = check_tensor(conv_weight, "conv_weight", 2, sw, SSD_F32, true, false))) return st;
@@ -703,17 +710,21 @@ ssd_status ssd_mixer_prologue(const ssd_tensor *xBC, const ssd_tensor *conv_weig
     if ((st = check_tensor(Bm, "B", 4, sbc, xdt, false, true))) return st;
     if ((st = check_tensor(Cm, "C", 4, sbc, xdt, false, true))) return st;
     if ((st = check_tensor(dt_out, "dt_out", 3, sdt, SSD_F32, false, false))) return st;
+    if (conv_state_indices && (st = check_tensor(conv_state_indices, "conv_state_indices", 1,
+                                                 sslot, SSD_I32, true, false)))
+        return st;
 
     // every output against every input and each other; the conv state is
     // updated in place, so it may overlap nothing else
     const Range ins[] = {range_of(xBC), range_of(conv_weight), range_of(conv_bias),
-                         range_of(dt), range_of(dt_bias)};
-    const char *in_names[] = {"xBC", "conv_weight", "conv_bias", "dt", "dt_bias"};
+                         range_of(dt), range_of(dt_bias), range_of(conv_state_indices)};
+    const char *in_names[] = {"xBC", "conv_weight", "conv_bias", "dt", "dt_bias",
+                              "conv_state_indices"};
     const Range outs[] = {range_of(x), range_of(Bm), range_of(Cm), range_of(dt_out),
                           range_of(conv_state), range_of(conv_windows)};
     const char *out_names[] = {"x", "B", "C", "dt_out", "conv_state", "conv_windows"};
     for (int o = 0; o < 6; ++o) {
-        for (int i = 0; i < 5; ++i)
+        for (int i = 0; i < 6; ++i)
             if (overlap(outs[o], ins[i]))
                 return fail(SSD_ERR_INVALID_ARG, "%s overlaps %s", out_names[o], in_names[i]);
         for (int o2 = o + 1; o2 < 6; ++o2)
@@ -726,7 +737,8 @@ ssd_status ssd_mixer_prologue(const ssd_tensor *xBC, const ssd_tensor *conv_weig
                                  {dp(conv_bias), "conv_bias"}, {dp(conv_state), "conv_state"},
                                  {dp(conv_windows), "conv_windows"}, {dp(dt), "dt"},
                                  {dp(dt_bias), "dt_bias"}, {dp(x), "x"}, {dp(Bm), "B"},
-                                 {dp(Cm), "C"}, {dp(dt_out), "dt_out"}})))
+                                 {dp(Cm), "C"}, {dp(dt_out), "dt_out"},
+                                 {dp(conv_state_indices), "conv_state_indices"}})))
         return st;
     ssd::MixerArgs a;
     a.B = int(Bn);
@@ -746,6 +758,9 @@ ssd_status ssd_mixer_prologue(const ssd_tensor *xBC, const ssd_tensor *conv_weig
     a.conv_b = conv_bias ? static_cast<const float *>(conv_bias->data) : nullptr;
     a.state = conv_state ? conv_state->data : nullptr;
     a.windows = conv_windows ? conv_windows->data : nullptr;
+    a.slots = conv_state_indices ? static_cast<const int32_t *>(conv_state_indices->data)
+                                 : nullptr;
+    a.S = int(S);
     a.dt = static_cast<const float *>(dt->data);
     a.dt_sb = dt->stride[0];
     a.dt_sl = dt->stride[1];

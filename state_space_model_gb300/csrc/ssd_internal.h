@@ -86,6 +86,8 @@ struct MixerArgs {
     const float *conv_b = nullptr;            // may be null (= 0)
     void *state = nullptr;                    // may be null (zero context, not written)
     void *windows = nullptr;                  // may be null
+    const int32_t *slots = nullptr;           // may be null (row b uses state b)
+    int S = 0;                                // slots in the state / windows pools
     const float *dt = nullptr;  int64_t dt_sb = 0, dt_sl = 0;
     const float *dt_bias = nullptr;           // may be null (= 0)
     float *dt_out = nullptr;    int64_t do_sb = 0, do_sl = 0;

@@ -103,12 +103,19 @@ __device__ __forceinline__ T *dest(const MixerArgs &a, int b, int c0, int64_t &s
 // [r run, + run), kUnroll token vectors in flight at a time.  The CTAs of a
 // run also share the dt preparation of its tokens, an equal slice each.  The conv state is written here only when one
 // run covers the sequence (gridDim.y = 1), so the thread that read a state
-// entry is the one that overwrites it.
+// entry is the one that overwrites it.  With slot indices row b's conv state
+// and windows are slot slots[b] of their pools, and a row whose slot is outside
+// the pool is padding: nothing is read or written for it.
 template <typename T, int W, bool kWindows>
 __global__ void __launch_bounds__(kConvMaxThreads)
 k_conv_prologue(const MixerArgs a, int64_t run) {
     constexpr int V = Vec<T>::kN;
     const int b = blockIdx.z;
+    int64_t slot = b;
+    if (a.slots) {
+        slot = a.slots[b];
+        if (slot < 0 || slot >= a.S) return;
+    }
     const int64_t t0 = int64_t(blockIdx.y) * run;
     const int64_t t1 = t0 + run < a.L ? t0 + run : a.L;
     const bool write_state = gridDim.y == 1;
@@ -137,7 +144,7 @@ k_conv_prologue(const MixerArgs a, int64_t run) {
         for (int k = 0; k < W; ++k) w[k][j] = a.conv_w[int64_t(c0 + j) * W + k];
     }
     const T *xin = static_cast<const T *>(a.xBC) + int64_t(b) * a.in_sb + c0;
-    T *state = a.state ? static_cast<T *>(a.state) + (int64_t(b) * a.Dc + c0) * W : nullptr;
+    T *state = a.state ? static_cast<T *>(a.state) + (slot * a.Dc + c0) * W : nullptr;
 
     // win[k] = input t - (W - 1) + k for the token t about to be computed;
     // win[W - 1] is filled from token t itself
@@ -172,7 +179,7 @@ k_conv_prologue(const MixerArgs a, int64_t run) {
         }
         Vec<T>::store(dst + t * dsl, o);
         if constexpr (kWindows) {   // the state after token t: its last W inputs
-            T *wp = static_cast<T *>(a.windows) + ((int64_t(b) * a.L + t) * a.Dc + c0) * W;
+            T *wp = static_cast<T *>(a.windows) + ((slot * a.L + t) * a.Dc + c0) * W;
 #pragma unroll
             for (int j = 0; j < V; ++j)
 #pragma unroll
@@ -220,9 +227,14 @@ __global__ void __launch_bounds__(256) k_conv_state_tail(const MixerArgs a) {
     const int b = blockIdx.y;
     const int i = blockIdx.x * 256 + threadIdx.x;   // (channel, column) of the state
     if (i >= a.Dc * W) return;
+    int64_t slot = b;
+    if (a.slots) {
+        slot = a.slots[b];
+        if (slot < 0 || slot >= a.S) return;        // a padding row
+    }
     const int c = i / W, k = i % W;
     const T *xin = static_cast<const T *>(a.xBC) + int64_t(b) * a.in_sb;
-    static_cast<T *>(a.state)[int64_t(b) * a.Dc * W + i] = xin[(a.L - W + k) * a.in_sl + c];
+    static_cast<T *>(a.state)[slot * a.Dc * W + i] = xin[(a.L - W + k) * a.in_sl + c];
 }
 
 int sm_count() {

@@ -180,15 +180,18 @@ def state_update_tokens(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_
 
 
 def mixer_prologue(xBC, conv_weight, dt, nheads, headdim, ngroups, dstate, *, conv_bias=None,
-                   conv_state=None, conv_windows=None, dt_bias=None, dt_softplus=True,
-                   out=None):
+                   conv_state=None, conv_windows=None, conv_state_indices=None, dt_bias=None,
+                   dt_softplus=True, out=None):
     """Causal conv1d + SiLU over xBC [B,L,Dc], split into x [B,L,H,P], B and C
     [B,L,G,N], and dt' = softplus(dt + dt_bias) [B,L,H] f32
     (``ssd_mixer_prologue``).  ``conv_state`` [B,Dc,W] is read as the left
     context and updated in place; ``conv_windows`` [B,L,Dc,W] receives the
-    window after every token.  Returns ``(x, B, C, dt')``; ``out`` may give
-    those four buffers."""
-    dev = _device_of(xBC, conv_weight, dt, conv_bias, conv_state, conv_windows, dt_bias)
+    window after every token.  ``conv_state_indices`` [B] int32 makes both
+    pools of S slots ([S,Dc,W], [S,L,Dc,W]), row b on slot
+    conv_state_indices[b]; rows with an index outside [0, S) are skipped.
+    Returns ``(x, B, C, dt')``; ``out`` may give those four buffers."""
+    dev = _device_of(xBC, conv_weight, dt, conv_bias, conv_state, conv_windows,
+                     conv_state_indices, dt_bias)
     Bn, L, _ = xBC.shape
     if out is None:
         out = (torch.empty((Bn, L, nheads, headdim), dtype=xBC.dtype, device=dev),
@@ -198,7 +201,8 @@ def mixer_prologue(xBC, conv_weight, dt, nheads, headdim, ngroups, dstate, *, co
     x, Bm, Cm, dt_out = out
     _device_of(x, Bm, Cm, dt_out)
     st = _native.load().ssd_mixer_prologue(_desc(xBC), _desc(conv_weight), _desc(conv_bias),
-                                           _desc(conv_state), _desc(conv_windows), _desc(dt),
+                                           _desc(conv_state), _desc(conv_windows),
+                                           _desc(conv_state_indices), _desc(dt),
                                            _desc(dt_bias), 1 if dt_softplus else 0, ngroups,
                                            _desc(x), _desc(Bm), _desc(Cm), _desc(dt_out),
                                            _stream(dev))

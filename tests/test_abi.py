@@ -369,3 +369,34 @@ def test_state_update_tokens_error_paths(lib):
 def test_selftest_wait_limit_is_checked_on_the_host(lib):
     assert lib.ssd_selftest_wait_timeout(200_000_000, None) == 1
     assert "100 ms" in detail(lib)
+
+
+def test_mixer_prologue_slot_checks(lib):
+    """ssd_mixer_prologue's host checks for conv-state slots (fake pointers)."""
+    p = ctypes.pointer
+    I32 = 2
+    Bn, L, H, P, G, N, W, S = 2, 8, 2, 64, 1, 128, 4, 5
+    Dc = H * P + 2 * G * N
+    base = FAKE + (1 << 35)
+    xbc = tens((Bn, L, Dc), BF16, ptr=base)
+    w = tens((Dc, W), F32, ptr=base + (1 << 24))
+    dt = tens((Bn, L, H), F32, ptr=base + (2 << 24))
+    x = tens((Bn, L, H, P), BF16, ptr=base + (3 << 24))
+    Bm = tens((Bn, L, G, N), BF16, ptr=base + (4 << 24))
+    Cm = tens((Bn, L, G, N), BF16, ptr=base + (5 << 24))
+    dto = tens((Bn, L, H), F32, ptr=base + (6 << 24))
+    pool = tens((S, Dc, W), BF16, ptr=base + (7 << 24))
+    slots = tens((Bn,), I32, ptr=base + (8 << 24))
+
+    def call(state=pool, idx=slots, windows=None):
+        q = lambda t: None if t is None else p(t)
+        return lib.ssd_mixer_prologue(p(xbc), p(w), None, q(state), q(windows), q(idx), p(dt),
+                                      None, 1, G, p(x), p(Bm), p(Cm), p(dto), None)
+
+    assert call(state=None) == 1 and "needs conv_state" in detail(lib)
+    assert call(idx=None) == 1 and "conv_state: shape[0]" in detail(lib)   # a pool needs slots
+    assert call(idx=tens((Bn,), F32, ptr=slots.data)) == 1 and "dtype" in detail(lib)
+    assert call(idx=tens((Bn + 1,), I32, ptr=slots.data)) == 1 and "shape" in detail(lib)
+    assert call(windows=tens((Bn, L, Dc, W), BF16, ptr=base + (9 << 24))) == 1 and \
+        "conv_windows: shape[0]" in detail(lib)                             # windows: a pool too
+    assert call(idx=tens((Bn,), I32, ptr=pool.data)) == 1 and "overlaps" in detail(lib)

@@ -155,3 +155,57 @@ def test_gated_forward_matches_oracle(ssd, case):
     bar = 2e-2 if dtype == torch.bfloat16 else 1e-4
     assert rel(y.double().cpu().numpy(), yg_ref) <= bar
     assert rel(fin.double().cpu().numpy(), fin_ref) <= bar
+
+
+SLOT_CASES = [
+    # (B, S, L, H, P, G, N, W, dtype, windows)
+    (5, 8, 300, 4, 64, 2, 128, 4, torch.bfloat16, False),   # several runs: the tail kernel
+    (4, 6, 3, 4, 64, 1, 128, 4, torch.bfloat16, True),      # decode-sized calls, windows
+    (3, 5, 40, 2, 32, 1, 16, 3, torch.float32, True),
+]
+
+
+@pytest.mark.parametrize("case", SLOT_CASES, ids=lambda c: f"B{c[0]}S{c[1]}L{c[2]}W{c[7]}"
+                         f"-{str(c[8])[6:]}-win{int(c[9])}")
+def test_mixer_prologue_slots_match_oracle(ssd, case):
+    """Conv-state slots: real rows match the oracle on their slots, padding rows
+    leave every output untouched, other slots and their windows are unchanged."""
+    B, S, L, H, P, G, N, W, dtype, windows = case
+    inp = make_mixer(B, L, H, P, G, N, W, dtype, seed=S * 11 + L, state=False)
+    Dc = H * P + 2 * G * N
+    g = torch.Generator().manual_seed(S + L)
+    pool = torch.randn((S, Dc, W), generator=g).to(dtype)
+    idx = torch.randperm(S, generator=g)[:B].to(torch.int32)
+    idx[0], idx[-1] = S + 1, -1                 # two padding rows
+    out_ref, st_ref, win_ref = orc.causal_conv1d(inp["xBC"], inp["conv_weight"],
+                                                 inp["conv_bias"], pool, state_indices=idx)
+    x_ref, b_ref, c_ref = orc.split_xbc(out_ref, H, P, G, N)
+    dt_ref = orc.dt_prologue(inp["dt"], inp["dt_bias"], True)
+    d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    state = pool.cuda()
+    win = torch.full((S, L, Dc, W), 5.0, dtype=dtype, device="cuda") if windows else None
+    outs = (torch.full((B, L, H, P), 9.0, dtype=dtype, device="cuda"),
+            torch.full((B, L, G, N), 9.0, dtype=dtype, device="cuda"),
+            torch.full((B, L, G, N), 9.0, dtype=dtype, device="cuda"),
+            torch.full((B, L, H), 9.0, dtype=torch.float32, device="cuda"))
+    x, Bm, Cm, dt = ssd.mixer_prologue(d["xBC"], d["conv_weight"], d["dt"], H, P, G, N,
+                                       conv_bias=d["conv_bias"], conv_state=state,
+                                       conv_windows=win, conv_state_indices=idx.cuda(),
+                                       dt_bias=d["dt_bias"], out=outs)
+    torch.cuda.synchronize()
+    real = [b for b in range(B) if 0 <= int(idx[b]) < S]
+    used = [int(idx[b]) for b in real]
+    bar = 2e-2 if dtype == torch.bfloat16 else 1e-4
+    for got, ref in ((x, x_ref), (Bm, b_ref), (Cm, c_ref)):
+        got = got.double().cpu().numpy()
+        assert rel(got[real], ref[real]) <= bar
+        assert np.all(got[[0, B - 1]] == 9.0)
+    dtg = dt.double().cpu().numpy()
+    assert rel(dtg[real], dt_ref[real]) <= 1e-5 and np.all(dtg[[0, B - 1]] == 9.0)
+    cast = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dtype)
+    assert torch.equal(state.cpu(), cast(st_ref))           # used slots replaced, others kept
+    if windows:
+        wg = win.cpu()
+        assert torch.equal(wg[used], cast(win_ref[real]))
+        unused = sorted(set(range(S)) - set(used))
+        assert torch.all(wg[unused] == 5.0)

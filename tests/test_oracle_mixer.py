@@ -177,3 +177,30 @@ def test_conv_pins_reject_planted_mistakes(mistake):
     o_ref, n_ref, _ = orc.causal_conv1d(**inp)
     np.testing.assert_allclose(o2, o_ref, rtol=1e-14, atol=1e-14)
     np.testing.assert_array_equal(n2, n_ref)
+
+
+@pytest.mark.parametrize("indices", [[4, -1, 1], [0, 2, 9]], ids=["pad_negative", "pad_past_end"])
+def test_conv_slots_run_each_row_on_its_slot(indices):
+    """A conv-state pool: each real row equals numpy's convolution of that row
+    preceded by its slot's inputs, its slot is replaced by the row's last W
+    inputs, other slots are unchanged and padding rows are not computed."""
+    S, W = 5, 4
+    inp = rand_conv(B=3, L=7, W=W, seed=21)
+    g = torch.Generator().manual_seed(22)
+    pool = torch.randn((S, 6, W), generator=g, dtype=f64)
+    out, new, win = orc.causal_conv1d(**dict(inp, conv_state=pool), silu=False,
+                                      state_indices=torch.tensor(indices, dtype=torch.int32))
+    x, w, b = inp["xBC"].numpy(), inp["weight"].numpy(), inp["bias"].numpy()
+    used = set()
+    for bb, slot in enumerate(indices):
+        if not 0 <= slot < S:
+            assert np.all(np.isnan(out[bb])) and np.all(np.isnan(win[bb]))
+            continue
+        used.add(slot)
+        for c in range(x.shape[2]):
+            u = np.concatenate([pool[slot, c].numpy(), x[bb, :, c]])
+            ref = np.convolve(u, w[c][::-1], mode="valid")[1:] + b[c]
+            np.testing.assert_allclose(out[bb, :, c], ref, rtol=1e-13, atol=1e-13)
+            np.testing.assert_array_equal(new[slot, c], u[-W:])
+    for slot in set(range(S)) - used:
+        np.testing.assert_array_equal(new[slot], pool[slot].numpy())
