@@ -209,3 +209,29 @@ def test_mixer_prologue_slots_match_oracle(ssd, case):
         assert torch.equal(wg[used], cast(win_ref[real]))
         unused = sorted(set(range(S)) - set(used))
         assert torch.all(wg[unused] == 5.0)
+
+
+def test_prologue_benchmark_shape_sampled(ssd):
+    """The prologue benchmark's call (Mamba-2 2.7B mixer shape: batch 8, 4096
+    tokens, 5376 channels, width 4, conv state in place, bias, softplus) with
+    its seeded inputs; every output of two sampled sequences checked against
+    the oracle (the convolution is independent per sequence)."""
+    from state_space_model_gb300 import inputs as gen
+    w = gen.WORKLOADS["mamba2_2p7b"]
+    Bn, L, H, P, G, N, W = w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, 4
+    cpu = gen.make_prologue_inputs(Bn, L, H, P, G, N, W, seed=20280)
+    d = {k: v.cuda() for k, v in cpu.items()}
+    x, Bm, Cm, dt = ssd.mixer_prologue(d["xBC"], d["conv_weight"], d["dt"], H, P, G, N,
+                                       conv_bias=d["conv_bias"], conv_state=d["conv_state"],
+                                       dt_bias=d["dt_bias"], dt_softplus=True)
+    torch.cuda.synchronize()
+    rows = [2, 7]
+    out_ref, st_ref, _ = orc.causal_conv1d(cpu["xBC"][rows], cpu["conv_weight"],
+                                           cpu["conv_bias"], cpu["conv_state"][rows])
+    x_ref, b_ref, c_ref = orc.split_xbc(out_ref, H, P, G, N)
+    for got, ref in ((x, x_ref), (Bm, b_ref), (Cm, c_ref)):
+        assert rel(got[rows].double().cpu().numpy(), ref) <= 2e-2
+    dt_ref = orc.dt_prologue(cpu["dt"][rows], cpu["dt_bias"], True)
+    assert rel(dt[rows].double().cpu().numpy(), dt_ref) <= 1e-5
+    cast = torch.from_numpy(np.ascontiguousarray(st_ref)).to(torch.bfloat16)
+    assert torch.equal(d["conv_state"][rows].cpu(), cast)

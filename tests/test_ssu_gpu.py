@@ -383,3 +383,48 @@ def test_state_slots_match_oracle(ssd, case):
         ic = inter.double().cpu().numpy()
         assert rel(ic[used], cache_ref[real]) <= (1e-2 if bf else 1e-4)
         assert np.all(ic[unused] == 3.0)
+
+
+# ---- the benchmark's shape and launch, sampled --------------------------------
+
+@pytest.mark.parametrize("T,sdt", [(1, torch.float32), (1, torch.bfloat16), (4, torch.float32),
+                                   (4, torch.bfloat16)], ids=["T1-f32", "T1-bf16", "T4-f32",
+                                                              "T4-bf16"])
+def test_decode_benchmark_shape_sampled(ssd, T, sdt):
+    """The decode benchmark's inputs (batch 64, 128 heads, P 64, N 128, 8 groups,
+    gated, dt bias + softplus; four tokens keep the cache) through the same
+    calls; outputs, states and cache checked on sampled sequences against the
+    oracle."""
+    from state_space_model_gb300 import inputs as gen
+    sh = gen.SSU_SHAPE
+    Bn, H, P, N, G = sh["batch"], sh["nheads"], sh["headdim"], sh["dstate"], sh["ngroups"]
+    cpu = gen.make_ssu_inputs(Bn, H, P, N, G, seed=20270, tokens=T if T > 1 else None)
+    cpu["state"] = cpu["state"].to(sdt)
+    d = {k: (None if v is None else v.cuda()) for k, v in cpu.items()}
+    state = d["state"].clone()
+    kw = dict(D=d["D"], z=d["z"], dt_bias=d["dt_bias"], dt_softplus=True, ngroups=G)
+    if T > 1:
+        inter = torch.empty((Bn, T, H, P, N), dtype=sdt, device="cuda")
+        out = ssd.state_update_tokens(state, d["x"], d["dt"], d["A"], d["B"], d["C"],
+                                      intermediate_states=inter, **kw)
+    else:
+        inter = None
+        out = ssd.state_update(state, d["x"], d["dt"], d["A"], d["B"], d["C"], **kw)
+    torch.cuda.synchronize()
+    rows = [0, 29, 63]
+    sel = lambda t: None if t is None else t[rows]
+    tk = (lambda t: t) if T > 1 else (lambda t: None if t is None else t.unsqueeze(1))
+    bf = sdt == torch.bfloat16
+    out_ref, fin_ref, cache_ref = orc.ssu_tokens(
+        sel(cpu["state"]), tk(sel(cpu["x"])), tk(sel(cpu["dt"])), cpu["A"], tk(sel(cpu["B"])),
+        tk(sel(cpu["C"])), D=cpu["D"], z=tk(sel(cpu["z"])), dt_bias=cpu["dt_bias"],
+        dt_softplus=True, ngroups=G, state_dtype="bf16" if bf else None)
+    got = out[rows].double().cpu().numpy()
+    assert rel(got if T > 1 else got[:, None], out_ref) <= 2e-2
+    st = state[rows].double().cpu().numpy()
+    if bf and T == 1:
+        bf16_step_check(st, fin_ref, 0.99)
+    else:
+        assert rel(st, fin_ref) <= (1e-2 if bf else 1e-4)
+    if inter is not None:
+        assert rel(inter[rows].double().cpu().numpy(), cache_ref) <= (1e-2 if bf else 1e-4)
