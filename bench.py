@@ -159,10 +159,11 @@ class ClockSampler:
 
 # the sources each recorded kernel is built from (a change elsewhere leaves
 # its DRAM traffic record valid)
-KERNEL_SOURCES = {
-    "ssd_fused": ["ssd_fused.cu", "ptx_sm100.cuh", "ssd_tc.cuh", "ssd_internal.h"],
-    "k_ssu_tokens": ["ssd_ssu.cu", "ptx_sm100.cuh", "ssd_internal.h"],
-    "k_conv_prologue": ["ssd_mixer.cu", "ssd_internal.h"],
+KERNEL_SOURCES = {   # each kernel's translation unit and the headers it includes
+    "ssd_fused": ["ssd_fused.cu", "ptx_sm100.cuh", "ssd_tc.cuh", "ssd_tmap.h", "ssd_internal.h",
+                  "ssd_common.h"],
+    "k_ssu_tokens": ["ssd_ssu.cu", "ptx_sm100.cuh", "ssd_decode.h", "ssd_common.h"],
+    "k_conv_prologue": ["ssd_mixer.cu", "ssd_mixer.h", "ssd_common.h"],
 }
 
 

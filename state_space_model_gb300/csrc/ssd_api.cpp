@@ -3,7 +3,9 @@
 // stream.  Every check runs before the first launch; nothing here allocates,
 // frees or synchronises.
 #include "ssd.h"
+#include "ssd_decode.h"
 #include "ssd_internal.h"
+#include "ssd_mixer.h"
 #include "ssd_tc.cuh"
 
 #include <cstdarg>

@@ -5,8 +5,7 @@
 // in flight when it gives up (no copy, no tensor-core work), so the context
 // stays usable.
 #include "ptx_sm100.cuh"
-#include "ssd_internal.h"
-#include "ssd_tc.cuh"
+#include "ssd_common.h"
 
 #include <cuda_runtime.h>
 

@@ -29,8 +29,7 @@
 // output is a shuffle reduction over the lanes holding it.  No tensor cores:
 // the only contraction is a length-N dot product per row.
 #include "ptx_sm100.cuh"
-#include "ssd_internal.h"
-#include "ssd_tc.cuh"
+#include "ssd_decode.h"
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

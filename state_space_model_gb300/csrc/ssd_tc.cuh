@@ -3,8 +3,6 @@
 #include "ssd_internal.h"
 
 namespace ssd {
-// Device address of the per-device error word that bounded waits set.
-cudaError_t device_error_word(unsigned int **out);
 
 bool tc_chunk_state_supported(const Args &a);
 cudaError_t tc_chunk_state(const Args &a, cudaStream_t s);
