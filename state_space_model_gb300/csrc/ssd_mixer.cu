@@ -107,8 +107,7 @@ __device__ __forceinline__ T *dest(const MixerArgs &a, int b, int c0, int64_t &s
 // and windows are slot slots[b] of their pools, and a row whose slot is outside
 // the pool is padding: nothing is read or written for it.
 template <typename T, int W, bool kWindows>
-__global__ void __launch_bounds__(kConvMaxThreads)
-k_conv_prologue(const MixerArgs a, int64_t run) {
+__device__ __forceinline__ void conv_prologue(const MixerArgs &a, int64_t run) {
     constexpr int V = Vec<T>::kN;
     const int b = blockIdx.z;
     int64_t slot = b;
@@ -220,6 +219,19 @@ k_conv_prologue(const MixerArgs a, int64_t run) {
     }
 }
 
+// Without windows the loads in flight per SM are the limit: 72 registers fit
+// four 224-thread CTAs per SM where the unconstrained 74 fit three (0.172 ->
+// 0.151 ms at the 2.7B shape).  With windows more values stay live, so no cap.
+template <typename T, int W>
+__global__ void __maxnreg__(72) k_conv_prologue(const MixerArgs a, int64_t run) {
+    conv_prologue<T, W, false>(a, run);
+}
+template <typename T, int W>
+__global__ void __launch_bounds__(kConvMaxThreads) k_conv_prologue_windows(const MixerArgs a,
+                                                                           int64_t run) {
+    conv_prologue<T, W, true>(a, run);
+}
+
 // The conv state after a sequence of L > 8 >= W tokens: its last W inputs
 // (read only from xBC, so it runs after the main launch has read the old state).
 template <typename T, int W>
@@ -255,7 +267,7 @@ cudaError_t launch_w(const MixerArgs &a, cudaStream_t s) {
     const int nvec = a.Dc / V;
     const int nbx = (nvec + kConvMaxThreads - 1) / kConvMaxThreads;
     const int threads = ((nvec + nbx - 1) / nbx + 31) / 32 * 32;
-    auto kern = a.windows ? k_conv_prologue<T, W, true> : k_conv_prologue<T, W, false>;
+    auto kern = a.windows ? k_conv_prologue_windows<T, W> : k_conv_prologue<T, W>;
     // each sequence split into R runs so that the grid is one wave of
     // resident CTAs (no tail wave); runs of at least 8 tokens
     int per_sm = 0;
