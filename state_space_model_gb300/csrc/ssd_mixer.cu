@@ -27,7 +27,7 @@ namespace ssd {
 namespace {
 
 constexpr int kConvMaxThreads = 256;
-constexpr int kUnroll = 8;   // token vectors loaded before any is used
+constexpr int kUnroll = 10;   // token vectors loaded before any is used
 
 template <typename T>
 struct Vec;   // one 8-byte vector of channels (few registers per thread, so
@@ -220,8 +220,9 @@ __device__ __forceinline__ void conv_prologue(const MixerArgs &a, int64_t run) {
 }
 
 // Without windows the loads in flight per SM are the limit: 72 registers fit
-// four 224-thread CTAs per SM where the unconstrained 74 fit three (0.172 ->
-// 0.151 ms at the 2.7B shape).  With windows more values stay live, so no cap.
+// four 224-thread CTAs per SM where the unconstrained 74 fit three, with ten
+// token vectors in flight per thread (0.172 -> 0.145 ms at the 2.7B shape).
+// With windows more values stay live, so no cap.
 template <typename T, int W>
 __global__ void __maxnreg__(72) k_conv_prologue(const MixerArgs a, int64_t run) {
     conv_prologue<T, W, false>(a, run);
