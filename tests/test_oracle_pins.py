@@ -2,7 +2,8 @@
 
 Each check ties one part of the oracle to something the pages or the
 mathematics fix: hand-derived worked examples (tests/golden/), the decay-free
-closed form (causal linear attention), the dt = 0 invariant, the scalar
+closed form (causal linear attention), the geometric-series closed form
+for inputs held constant, the dt = 0 invariant, the scalar
 first-order recurrence, chunk-size invariance of the chunked form, the state
 hand-off (resumability) and linearity.  ``test_pins_reject_planted_mistakes``
 shows that a plausible mistake (an index, a sign, a dropped term, a transposed
@@ -148,6 +149,46 @@ def test_decay_free_closed_form():
             assert rel(y[b, :, h, :], Y) < 1e-12
             F = h0[b, h] + (dt[b, :, h][:, None] * x[b, :, h, :]).T @ Bg
             assert rel(f[b, h], F) < 1e-12
+
+
+@pytest.mark.parametrize("form", ["recurrence", "chunked"])
+def test_constant_inputs_geometric_series(form):
+    """Inputs held constant over the sequence (x per (b, h); B, C per
+    (b, g); dt per head): the recurrence is a geometric series, so after
+    token t (counting from 0), with alpha = exp(A dt),
+        S_t = alpha^(t+1) H0 + dt x b^T (1 - alpha^(t+1)) / (1 - alpha),
+        y_t = S_t c + D x.
+    Long sequences with decays from 0.37 to 0.9995 per token exercise the
+    decay far beyond the hand-derived examples, on both oracle forms (the
+    chunked one with a partial last chunk)."""
+    Bn, L, H, P, N, G = 2, 300, 4, 3, 5, 2
+    g = torch.Generator().manual_seed(31)
+    r = lambda *s: torch.randn(s, generator=g, dtype=f64)
+    xc, bc, cc, h0, D = r(Bn, H, P), r(Bn, G, N), r(Bn, G, N), r(Bn, H, P, N), r(H)
+    dtc = torch.tensor([0.05, 0.5, 0.01, 0.25], dtype=f64)
+    A = torch.tensor([-0.01, -2.0, -0.05, -1.0], dtype=f64)
+    inp = dict(x=xc[:, None].expand(Bn, L, H, P).contiguous(),
+               dt=dtc.expand(Bn, L, H).contiguous(), A=A,
+               Bm=bc[:, None].expand(Bn, L, G, N).contiguous(),
+               Cm=cc[:, None].expand(Bn, L, G, N).contiguous(), D=D, h0=h0, ngroups=G)
+    if form == "recurrence":
+        y, f = orc.recurrence(**inp)
+    else:
+        out = orc.chunked(**inp, chunk_size=64)
+        y = out["y"].reshape(Bn, H, L, P).transpose(0, 2, 1, 3)
+        f = out["final"].reshape(Bn, H, P, N)
+    t1 = np.arange(1, L + 1, dtype=np.float64)
+    for b in range(Bn):
+        for h in range(H):
+            gi = h // (H // G)
+            alpha = math.exp(float(A[h] * dtc[h]))
+            pw = alpha ** t1                                              # alpha^(t+1)
+            geo = (1.0 - pw) / (1.0 - alpha)
+            inj = float(dtc[h]) * np.outer(xc[b, h].numpy(), bc[b, gi].numpy())
+            S = pw[:, None, None] * h0[b, h].numpy() + geo[:, None, None] * inj
+            Y = S @ cc[b, gi].numpy() + float(D[h]) * xc[b, h].numpy()
+            assert rel(y[b, :, h, :], Y) < 1e-11
+            assert rel(f[b, h], S[-1]) < 1e-11
 
 
 def test_dt_zero_keeps_state():
