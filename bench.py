@@ -167,14 +167,49 @@ KERNEL_SOURCES = {   # each kernel's translation unit and the headers it include
 }
 
 
+def code_tokens(src: str) -> str:
+    """C/C++/CUDA source with its comments removed and every run of
+    whitespace outside string and character literals collapsed to one space,
+    so that editing a comment or re-indenting leaves the result unchanged."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == "/" and src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif c == "/" and src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            if out and out[-1] != " ":
+                out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif c.isspace():
+            while i < n and src[i].isspace():
+                i += 1
+            if out and out[-1] != " ":
+                out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out).strip()
+
+
 def kernel_source_hash(stage: str) -> str:
+    """Hash of the code (comments and layout ignored) of the files a kernel
+    is built from: a recorded DRAM traffic figure stays valid while it holds."""
     csrc = os.path.join(ROOT, "state_space_model_gb300", "csrc")
     names = KERNEL_SOURCES.get(stage) or sorted(
         n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh", ".h")))
     h = hashlib.sha256()
     for name in names:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(code_tokens(f.read()).encode())
+        h.update(b"\0")
     return h.hexdigest()[:16]
 
 

@@ -26,16 +26,17 @@
 //
 // Only h(k + 1) = 2^(g_end) h(k) + S(k) is serial, and S(k) does not depend
 // on h, so every other product of a block is taken off that chain: S^T is
-// issued as soon as w o x is ready, the bf16 copy of the state is double
-// buffered (the next update does not wait for C h^T to read the current one),
-// and the state update, the decay operand and the y drain each have warps of
-// their own.  Blocks are software-pipelined across two stages of the buffers.
+// issued as soon as w o x is ready, and the state update, the decay operand
+// and the y drain each have warps of their own.  The bf16 copy of the state
+// that C h^T reads has one buffer: the update of block k writes it once
+// C h^T(k) has read it.  Blocks are software-pipelined across two stages of
+// the C, B and tensor-memory buffers.
 // Roles: warp 0 = TMA producer and the block's cumulative sum (published once
 // for every role), warp 1 = tensor-memory owner and MMA issuer, warps 2..7 =
 // warpgroup A (the decay operand L), warps 8..11 = warpgroup S (w o x and the
 // state), warps 12..15 = warpgroup Y (y and its TMA store).  A math thread
 // owns tile row / state row r = its TMEM lane.  One CTA per SM (all 512 TMEM
-// columns, 211 KB of shared memory).
+// columns, 216.4 KiB of shared memory).
 #include "ptx_sm100.cuh"
 #include "ssd_internal.h"
 #include "ssd_tc.cuh"

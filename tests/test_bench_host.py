@@ -97,3 +97,20 @@ def test_our_arm_refuses_to_run_without_a_gpu():
                        capture_output=True, text=True, timeout=300)
     assert r.returncode != 0
     assert "no CUDA device" in r.stderr
+
+
+def test_source_hash_ignores_comments_and_layout_only():
+    """A DRAM traffic record is keyed by a hash of the kernel's code: editing
+    a comment or re-indenting keeps it, any change of code (string literals
+    included) drops it."""
+    base = 'int f(int a) {\n    return a + 1;  // one\n}\nconst char *s = "a // b";\n'
+    same = ('/* doc */ int f(int a)\n{\n  return a + 1;   /* one */\n}\n'
+            'const char *s = "a // b";   // trailing\n')
+    assert bench.code_tokens(base) == bench.code_tokens(same)
+    for changed in (base.replace("+ 1", "+ 2"), base.replace('"a // b"', '"a //  b"'),
+                    base.replace("return a", "return  -a")):
+        assert bench.code_tokens(changed) != bench.code_tokens(base)
+    # every kernel that has a record hashes to a fixed-length hex string
+    for stage in bench.KERNEL_SOURCES:
+        h = bench.kernel_source_hash(stage)
+        assert len(h) == 16 and int(h, 16) >= 0
