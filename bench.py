@@ -694,15 +694,16 @@ def main():
     e2e = None
     if not args.no_e2e and not args.gate:   # (the gated line is a kernel measurement)
         host = {k: (None if v is None else v.pin_memory()) for k, v in inp_cpu.items()}
-        y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
-        f_h = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
         h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
-        d2h = y_h.numel() * y_h.element_size() + f_h.numel() * f_h.element_size()
+        d2h = y.numel() * y.element_size() + fin.numel() * fin.element_size()
 
-        # the batch in up to eight chunks through three streams -- uploads,
-        # scans, downloads, joined by events -- so chunk i + 1's upload, chunk
-        # i's scan and chunk i - 1's download run at once (the host <-> device
-        # copies dominate this measurement)
+        # Every step uploads its inputs, runs the forward and downloads y and
+        # final_states.  The batch goes through in up to eight chunks on three
+        # streams -- uploads, scans, downloads, joined by events -- so chunk
+        # i + 1's upload, chunk i's scan and chunk i - 1's download run at
+        # once; and consecutive steps use two sets of device and host buffers,
+        # so step j + 1's uploads run under step j's downloads (the host link
+        # carries both directions at once and bounds this measurement).
         nch = min(B, 8)
         cuts = [(B * i) // nch for i in range(nch + 1)]
         s_in, s_run, s_out = (torch.cuda.Stream(dev) for _ in range(3))
@@ -712,48 +713,68 @@ def main():
         ws_e2e = torch.empty(max(1, ssd.workspace_size(bmax, L, H, P, N, w.ngroups, w.chunk_size,
                                                        w.torch_dtype)),
                              dtype=torch.uint8, device=dev)
+        sets = []
+        for j in range(2):
+            dj = d if j == 0 else {k: (None if v is None else torch.empty_like(v))
+                                   for k, v in d.items()}
+            sets.append((dj, y if j == 0 else torch.empty_like(y),
+                         fin if j == 0 else torch.empty_like(fin),
+                         torch.empty(y.shape, dtype=y.dtype, pin_memory=True),
+                         torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)))
         ev_in = [torch.cuda.Event() for _ in range(nch)]
         ev_run = [torch.cuda.Event() for _ in range(nch)]
+        # per buffer set: its inputs consumed by its last scans, its outputs read back
+        ev_scanned = [torch.cuda.Event() for _ in range(2)]
+        ev_read = [torch.cuda.Event() for _ in range(2)]
+        for ev in ev_scanned + ev_read:
+            ev.record(stream)
 
-        def e2e_step():
-            for sd in (s_in, s_run, s_out):
-                sd.wait_stream(stream)        # after the previous step
+        def e2e_step(j):
+            dj, yj, fj, y_h, f_h = sets[j & 1]
+            s_in.wait_event(ev_scanned[j & 1])     # step j - 2's scans read these inputs
             with torch.cuda.stream(s_in):
                 for k in shared:
-                    d[k].copy_(host[k], non_blocking=True)
+                    dj[k].copy_(host[k], non_blocking=True)
                 for i in range(nch):
                     b0, b1 = cuts[i], cuts[i + 1]
                     for k in per_batch:
-                        d[k][b0:b1].copy_(host[k][b0:b1], non_blocking=True)
+                        dj[k][b0:b1].copy_(host[k][b0:b1], non_blocking=True)
                     ev_in[i].record(s_in)
+            s_run.wait_event(ev_read[j & 1])       # step j - 2's downloads read these outputs
             with torch.cuda.stream(s_run):
                 for i in range(nch):
                     b0, b1 = cuts[i], cuts[i + 1]
                     s_run.wait_event(ev_in[i])
-                    ssd.chunked_fwd(d["x"][b0:b1], d["dt"][b0:b1], d["A"], d["B"][b0:b1],
-                                    d["C"][b0:b1], d["D"],
-                                    None if d["initial_states"] is None
-                                    else d["initial_states"][b0:b1],
-                                    w.chunk_size, w.ngroups, y=y[b0:b1], final_states=fin[b0:b1],
-                                    workspace=ws_e2e)
+                    ssd.chunked_fwd(dj["x"][b0:b1], dj["dt"][b0:b1], dj["A"], dj["B"][b0:b1],
+                                    dj["C"][b0:b1], dj["D"],
+                                    None if dj["initial_states"] is None
+                                    else dj["initial_states"][b0:b1],
+                                    w.chunk_size, w.ngroups, y=yj[b0:b1],
+                                    final_states=fj[b0:b1], workspace=ws_e2e)
                     ev_run[i].record(s_run)
+                ev_scanned[j & 1].record(s_run)
             with torch.cuda.stream(s_out):
                 for i in range(nch):
                     b0, b1 = cuts[i], cuts[i + 1]
                     s_out.wait_event(ev_run[i])
-                    y_h[b0:b1].copy_(y[b0:b1], non_blocking=True)
-                    f_h[b0:b1].copy_(fin[b0:b1], non_blocking=True)
-            stream.wait_stream(s_out)
+                    y_h[b0:b1].copy_(yj[b0:b1], non_blocking=True)
+                    f_h[b0:b1].copy_(fj[b0:b1], non_blocking=True)
+                ev_read[j & 1].record(s_out)
+
+        def e2e_run(nsteps):
+            for sd in (s_in, s_run, s_out):
+                sd.wait_stream(stream)
+            for j in range(nsteps):
+                e2e_step(j)
+            stream.wait_stream(s_out)   # the downloads wait on every scan, the scans on every upload
 
         k_e2e = max(10, min(args.steps, 200))
-        for _ in range(3):
-            e2e_step()
+        e2e_run(3)
         torch.cuda.synchronize()
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(k_e2e):
-            e2e_step()
+        e2e_run(k_e2e)
         e1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -761,8 +782,9 @@ def main():
         e2e = {"value": world * tokens / (ems / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k_e2e,
                "ms_per_step": ems,
-               "pipelining": f"{nch} batch chunks through upload, scan and download "
-                             "streams (copies overlap the scan)"}
+               "pipelining": f"{nch} batch chunks through upload, scan and download streams; "
+                             "two buffer sets, so a step's uploads overlap the previous "
+                             "step's downloads"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
