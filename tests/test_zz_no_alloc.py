@@ -36,12 +36,24 @@ def rel(a, b):
     return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-30))
 
 
-def test_static_scratch_matches_workspace_entry_point(lib):
+# Both plans that need scratch memory: the four-step path (chunk 64, which
+# the single-kernel path does not take) and the single-kernel path's sequence
+# split (a few (batch, head) slabs over a long sequence).
+CASES = {
+    "four_step": dict(batch=2, seqlen=600, nheads=4, ngroups=2, chunk_size=64),
+    "sequence_split": dict(batch=1, seqlen=8000, nheads=4, ngroups=2, chunk_size=256),
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_static_scratch_matches_workspace_entry_point(lib, case):
     from state_space_model_gb300 import ssd
-    from state_space_model_gb300._native import SSD_BF16  # noqa: F401
-    # a shape that runs the four-step path, which needs scratch memory
-    w = gen.small_case("bf16", batch=2, seqlen=600, nheads=4, ngroups=2, chunk_size=64)
-    assert ssd.workspace_size(2, 600, 4, 64, 128, 2, 64, torch.bfloat16) > 0
+    w = gen.small_case("bf16", **CASES[case])
+    assert ssd.workspace_size(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups,
+                              w.chunk_size, torch.bfloat16) > 0
+    plan = ssd.describe_plan(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups,
+                             w.chunk_size, torch.bfloat16)
+    assert plan.startswith("staged" if case == "four_step" else "fused"), plan
     inp = {k: (None if v is None else v.cuda()) for k, v in gen.make_inputs(w).items()}
     y_ref, f_ref = ssd.chunked_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
                                    inp["initial_states"], w.chunk_size, w.ngroups)
