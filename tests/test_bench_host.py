@@ -114,3 +114,26 @@ def test_source_hash_ignores_comments_and_layout_only():
     for stage in bench.KERNEL_SOURCES:
         h = bench.kernel_source_hash(stage)
         assert len(h) == 16 and int(h, 16) >= 0
+
+
+def test_roofline_work_of_each_workload():
+    """The roofline's numerators: compulsory HBM bytes (x, B, C, dt, A, D and
+    the initial state read; y and the final state written) and flops (per
+    token and head 2NP chunk state + 2NP output from the state + (Q + 1)P on
+    the causal half of the intra-chunk product + 2NP/Q state pass, per token
+    and group (Q + 1)N for C B^T), worked out by hand for each workload."""
+    from state_space_model_gb300 import inputs as gen
+    # 2.7B layer: x = y = 8*4096*80*64*2 B = 335,544,320; B + C = 2*8*4096*128*2 =
+    # 16,777,216; dt = 8*4096*80*4 = 10,485,760; A + D = 640; final = 8*80*64*128*4
+    # = 20,971,520
+    expect_bytes = {"mamba2_2p7b": 2 * 335_544_320 + 16_777_216 + 10_485_760 + 640
+                    + 20_971_520}
+    b, f = bench.path_work(gen.WORKLOADS["mamba2_2p7b"])
+    assert b == expect_bytes["mamba2_2p7b"] == 719_323_776
+    T, H, P, N, Q, G = 8 * 4096, 80, 64, 128, 256, 1
+    assert f == T * H * (4 * N * P + (Q + 1) * P + 2 * N * P / Q) + T * G * (Q + 1) * N
+    # rounded figures of the other workloads (MB, GFLOP)
+    for name, mb, gf in [("tiny_f32", 0.172, 0.00239), ("mamba2_130m", 58.46, 9.96),
+                         ("hybrid_g8", 620.8, 88.47), ("long_64k", 2256.5, 417.7)]:
+        b, f = bench.path_work(gen.WORKLOADS[name])
+        assert abs(b / 1e6 - mb) / mb < 1e-3 and abs(f / 1e9 - gf) / gf < 1e-3, name
