@@ -3,7 +3,8 @@
 Each check ties one part of the oracle to something the pages or the
 mathematics fix: hand-derived worked examples (tests/golden/), the decay-free
 closed form (causal linear attention), the geometric-series closed form
-for inputs held constant, the dt = 0 invariant, the scalar
+for inputs held constant, scipy's first-order filter when the decay is
+constant, the dt = 0 invariant, the scalar
 first-order recurrence, chunk-size invariance of the chunked form, the state
 hand-off (resumability) and linearity.  ``test_pins_reject_planted_mistakes``
 shows that a plausible mistake (an index, a sign, a dropped term, a transposed
@@ -189,6 +190,33 @@ def test_constant_inputs_geometric_series(form):
             Y = S @ cc[b, gi].numpy() + float(D[h]) * xc[b, h].numpy()
             assert rel(y[b, :, h, :], Y) < 1e-11
             assert rel(f[b, h], S[-1]) < 1e-11
+
+
+def test_constant_decay_equals_scipy_lfilter():
+    """dt held constant per head (x, B and C still vary per token): every state
+    element follows the first-order filter s_t = alpha s_(t-1) + dt x_t[p] B_t[n]
+    with alpha = exp(A dt) and s_(-1) = H0[p, n], which scipy.signal.lfilter
+    computes ([1], [1, -alpha], with the initial condition alpha H0); then
+    y_t[p] = sum_n C_t[n] s_t[p, n] + D x_t[p].  Checks the outer-product
+    orientation, the head-to-group map and the contraction over n against a
+    library routine."""
+    signal = pytest.importorskip("scipy.signal")
+    Bn, L, H, P, N, G = 2, 200, 4, 3, 5, 2
+    inp = rand_inputs(B=Bn, L=L, H=H, P=P, N=N, G=G, seed=41)
+    dtc = torch.tensor([0.02, 0.3, 0.7, 0.1], dtype=f64)
+    inp["dt"] = dtc.expand(Bn, L, H).contiguous()
+    y, f = orc.recurrence(**inp)
+    x, Bm, Cm, D, h0, A = (inp[k].numpy() for k in ("x", "Bm", "Cm", "D", "h0", "A"))
+    for b in range(Bn):
+        for h in range(H):
+            g = h // (H // G)
+            alpha = math.exp(A[h] * float(dtc[h]))
+            u = float(dtc[h]) * x[b, :, h, :, None] * Bm[b, :, g, None, :]   # [L, P, N]
+            S, _ = signal.lfilter([1.0], [1.0, -alpha], u, axis=0,
+                                  zi=(alpha * h0[b, h])[None])
+            Y = np.einsum("tpn,tn->tp", S, Cm[b, :, g, :]) + D[h] * x[b, :, h, :]
+            assert rel(y[b, :, h, :], Y) < 1e-12
+            assert rel(f[b, h], S[-1]) < 1e-12
 
 
 def test_dt_zero_keeps_state():
