@@ -43,6 +43,11 @@
  * - Aliasing: outputs must not overlap inputs (checked by address range).
  * - Results are deterministic: repeated calls give bitwise-identical outputs
  *   (no floating-point atomics).
+ * - Device state: the library keeps two objects in device memory of its own
+ *   (a device error word, and the static scratch array of
+ *   ssd_chunked_fwd_static_scratch) and looks up their addresses once per
+ *   device, on first use.  cudaDeviceReset discards them, so do not reset a
+ *   device the library has been used on in the same process.
  */
 #ifndef SSD_GB300_H
 #define SSD_GB300_H
