@@ -156,7 +156,9 @@ Plan plan_workspace(const ssd::Dims &d, int xdt) {
     p.fused = ssd::use_fused(d, xdt);
     if (p.fused) {
         // only a split last wave needs scratch (the tail segments' states)
-        p.total = ssd::fused_split(d, ssd::device_sm_count()).ws_bytes;
+        p.total = (ssd::pair_supported(d, xdt) ? ssd::pair_split(d, ssd::device_sm_count())
+                                               : ssd::fused_split(d, ssd::device_sm_count()))
+                      .ws_bytes;
         return p;
     }
     const size_t g = size_t(d.B) * d.H * d.nc * d.Q * 4;
@@ -287,8 +289,23 @@ const char *ssd_describe_plan(int64_t batch, int64_t seqlen, int64_t nheads, int
     a.d = d;
     a.xdt = x_dtype;
     a.hprev_dt = x_dtype;
-    char buf[384];
-    if (ssd::use_fused(d, x_dtype)) {
+    char buf[512];
+    if (ssd::use_fused(d, x_dtype) && ssd::pair_supported(d, x_dtype)) {
+        const ssd::FusedSplit f = ssd::pair_split(d, ssd::device_sm_count());
+        if (f.nseg > 1)
+            snprintf(buf, sizeof buf,
+                     "fused: k_ssd_pair x %lld CTAs (%lld whole (batch, head pair) slabs + the "
+                     "last %lld pair slabs in %d segments of %lld tokens, after a states-only "
+                     "pass and a combine), two heads per CTA, 128-token blocks, tcgen05 + TMA, "
+                     "workspace %zu bytes",
+                     (long long)(f.n_whole + f.tail * f.nseg), (long long)f.n_whole,
+                     (long long)f.tail, f.nseg, (long long)f.seg_len, f.ws_bytes);
+        else
+            snprintf(buf, sizeof buf,
+                     "fused: k_ssd_pair x %lld CTAs ((batch, head pair) slabs), two heads per "
+                     "CTA, 128-token blocks, tcgen05 + TMA, no workspace",
+                     (long long)(batch * nheads / 2));
+    } else if (ssd::use_fused(d, x_dtype)) {
         const ssd::FusedSplit f = ssd::fused_split(d, ssd::device_sm_count());
         if (f.nseg > 1)
             snprintf(buf, sizeof buf,
@@ -447,7 +464,10 @@ ssd_status chunked_fwd_impl(const ssd_tensor *x, const ssd_tensor *dt, const ssd
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (plan.fused) {
-        if ((st = cuda_status(ssd::launch_fused(a, s), "fused forward"))) return st;
+        if ((st = cuda_status(ssd::pair_supported(a.d, xdt) ? ssd::launch_pair(a, s)
+                                                             : ssd::launch_fused(a, s),
+                              "fused forward")))
+            return st;
         if (z && (st = cuda_status(ssd::launch_gate(a, s), "output gate"))) return st;
         return ok();
     }

@@ -112,8 +112,9 @@ def detail(lib):
 
 def test_workspace_size(lib):
     out = ctypes.c_size_t()
-    # the fused single-kernel path needs no workspace
-    assert lib.ssd_workspace_size(8, 4096, 80, 64, 128, 1, 256, BF16, ctypes.byref(out)) == 0
+    # the fused path needs no workspace for whole waves of slabs (its split of
+    # the last partial wave is covered by test_fused_split_plan)
+    assert lib.ssd_workspace_size(2, 4096, 152, 64, 128, 1, 256, BF16, ctypes.byref(out)) == 0
     assert out.value == 0
     # the four-step path keeps G, S and h_prev there
     assert lib.ssd_workspace_size(8, 4096, 80, 64, 128, 1, 64, BF16, ctypes.byref(out)) == 0
@@ -138,33 +139,58 @@ def test_describe_plan(lib):
 
 
 def test_fused_split_plan(lib):
-    """Fewer (batch, head) slabs than SMs: the last wave is split by sequence.
+    """The pair slabs (or, for odd heads per group, the slabs) left over after
+    the last full wave of SMs are split by sequence.
 
     The plan names the segments; the workspace holds the tail segments' local
     states and decays and their entering states, each region 256-byte aligned.
-    A full wave or more of slabs is never split and needs no workspace.
+    A whole number of waves, or one 128-token block per slab, is never split
+    and needs no workspace.
     """
     import re
     d = lambda *a: lib.ssd_describe_plan(*a).decode()
     out = ctypes.c_size_t()
-    for B, L, H in [(1, 65536, 8), (1, 16384, 4), (1, 32768, 24), (2, 8000, 3)]:
+    a256 = lambda v: (v + 255) // 256 * 256
+    PN = 64 * 128
+    M = 152   # SM count assumed without a device
+    # (B, L, H, G): two heads per CTA (heads per group even)
+    for B, L, H, G in [(1, 65536, 8, 1), (1, 16384, 4, 1), (1, 32768, 24, 1), (8, 4096, 80, 1),
+                       (1, 16384, 128, 8)]:
+        plan = d(B, L, H, 64, 128, G, 256, BF16)
+        assert "k_ssd_pair" in plan, plan
+        m = re.search(r"(\d+) whole \(batch, head pair\) slabs \+ the last (\d+) pair slabs in "
+                      r"(\d+) segments of (\d+) tokens", plan)
+        assert m, plan
+        whole, tail, nseg, seg_len = map(int, m.groups())
+        assert whole + tail == B * H // 2 and whole % M == 0 and 0 < tail < M
+        assert nseg >= 2 and seg_len % 128 == 0
+        assert (nseg - 1) * seg_len < L <= nseg * seg_len
+        ws = a256(a256(a256(tail * (nseg - 1) * 2 * PN * 4) + tail * (nseg - 1) * 8) +
+                  tail * nseg * 2 * PN * 4)
+        assert lib.ssd_workspace_size(B, L, H, 64, 128, G, 256, BF16, ctypes.byref(out)) == 0
+        assert out.value == ws, (plan, out.value, ws)
+        assert f"workspace {ws} bytes" in plan
+    # one head per CTA (odd heads per group)
+    for B, L, H in [(1, 65536, 3), (2, 8000, 3), (1, 32768, 25)]:
         plan = d(B, L, H, 64, 128, 1, 256, BF16)
+        assert "k_ssd_fused" in plan, plan
         m = re.search(r"the last (\d+) slabs in (\d+) segments of (\d+) tokens", plan)
         assert m, plan
         tail, nseg, seg_len = map(int, m.groups())
         assert tail == B * H and nseg >= 2 and seg_len % 128 == 0
         assert (nseg - 1) * seg_len < L <= nseg * seg_len
-        a256 = lambda v: (v + 255) // 256 * 256
-        PN = 64 * 128
         ws = a256(a256(a256(tail * (nseg - 1) * PN * 4) + tail * (nseg - 1) * 4) + tail * nseg * PN * 4)
         assert lib.ssd_workspace_size(B, L, H, 64, 128, 1, 256, BF16, ctypes.byref(out)) == 0
         assert out.value == ws, (plan, out.value, ws)
         assert f"workspace {ws} bytes" in plan
-    # a full wave of slabs, or one 128-token block per slab: whole slabs only
-    for B, L, H in [(8, 4096, 80), (2, 65536, 80), (1, 128, 8)]:
-        assert "segments" not in d(B, L, H, 64, 128, 1, 256, BF16)
+    # whole waves of pair slabs, short pair slabs, or one block per slab: whole slabs only
+    for B, L, H in [(2, 4096, 152), (2, 640, 96), (1, 128, 8)]:
+        plan = d(B, L, H, 64, 128, 1, 256, BF16)
+        assert "segments" not in plan, plan
         assert lib.ssd_workspace_size(B, L, H, 64, 128, 1, 256, BF16, ctypes.byref(out)) == 0
         assert out.value == 0
+    assert "k_ssd_fused" in d(2, 4096, 153, 64, 128, 1, 256, BF16)   # odd heads per group
+    assert "k_ssd_pair" in d(2, 4096, 152, 64, 128, 1, 256, BF16)
 
 
 def test_error_paths(lib):
