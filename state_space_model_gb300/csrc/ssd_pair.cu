@@ -285,7 +285,6 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     const uint64_t now = ptx::globaltimer_ns();
                     if (!idle_since) idle_since = now;
                     else if (now - idle_since > 2000000000ull) fired = -1;
-                    else __nanosleep(64);
                 }
             }
             fired = __shfl_sync(0xffffffffu, fired, 0);
@@ -392,7 +391,6 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     const uint64_t now = ptx::globaltimer_ns();
                     if (!idle_since) idle_since = now;
                     else if (now - idle_since > 2000000000ull) { ok = false; break; }
-                    else __nanosleep(32);
                 }
             }
             // every product must land before tensor memory is released
@@ -457,19 +455,29 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             if constexpr (states_only) gsum += gend;
             const uint8_t *xt = smem + SM::kX + slot * 32768 + hh * 16384;
             uint8_t *wt = smem + SM::kW + hh * 16384;
+#pragma unroll 1
+            for (int i = 0; i < 4; i += 2) {
+                uint4 v[2][8];
+                __nv_bfloat162 wb[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = 32 * i + lane;
-                const float w = ex2(gend + rec[128 + r]);
-                const __nv_bfloat162 wb = __floats2bfloat162_rn(w, w);
+                for (int u = 0; u < 2; ++u) {
+                    const int r = 32 * (i + u) + lane;
+                    const float w = ex2(gend + rec[128 + r]);
+                    wb[u] = __floats2bfloat162_rn(w, w);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int off = r * 128 + ((c ^ (r & 7)) << 4);   // swizzled
-                    uint4 v = *reinterpret_cast<const uint4 *>(xt + off);
-                    __nv_bfloat162 *v2 = reinterpret_cast<__nv_bfloat162 *>(&v);
+                    for (int c = 0; c < 8; ++c)
+                        v[u][c] = *reinterpret_cast<const uint4 *>(xt + r * 128 + ((c ^ (r & 7)) << 4));
+                }
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) v2[kk] = __hmul2(v2[kk], wb);
-                    *reinterpret_cast<uint4 *>(wt + off) = v;
+                for (int u = 0; u < 2; ++u) {
+                    const int r = 32 * (i + u) + lane;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        __nv_bfloat162 *v2 = reinterpret_cast<__nv_bfloat162 *>(&v[u][c]);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) v2[kk] = __hmul2(v2[kk], wb[u]);
+                        *reinterpret_cast<uint4 *>(wt + r * 128 + ((c ^ (r & 7)) << 4)) = v[u][c];
+                    }
                 }
             }
             ptx::fence_proxy_async_smem();
