@@ -160,8 +160,10 @@ class ClockSampler:
 # the sources each recorded kernel is built from (a change elsewhere leaves
 # its DRAM traffic record valid)
 KERNEL_SOURCES = {   # each kernel's translation unit and the headers it includes
-    "ssd_fused": ["ssd_fused.cu", "ptx_sm100.cuh", "ssd_tc.cuh", "ssd_tmap.h", "ssd_internal.h",
-                  "ssd_common.h"],
+    "k_ssd_fused": ["ssd_fused.cu", "ssd_block_math.cuh", "ptx_sm100.cuh", "ssd_tc.cuh",
+                    "ssd_tmap.h", "ssd_internal.h", "ssd_common.h"],
+    "k_ssd_pair": ["ssd_pair.cu", "ssd_block_math.cuh", "ptx_sm100.cuh", "ssd_tc.cuh",
+                   "ssd_tmap.h", "ssd_internal.h", "ssd_common.h"],
     "k_ssu_tokens": ["ssd_ssu.cu", "ptx_sm100.cuh", "ssd_decode.h", "ssd_common.h"],
     "k_conv_prologue": ["ssd_mixer.cu", "ssd_mixer.h", "ssd_common.h"],
 }
@@ -618,6 +620,16 @@ def main():
         ev1.record(stream)
         torch.cuda.synchronize()
         ms = ev0.elapsed_time(ev1) / args.steps
+        # the spread: steps timed one by one (each its own event pair, back to
+        # back, no flush: the inputs exceed L2), after the timed window
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(max(50, min(args.steps, 200)))]
+        for ea, eb in evs:
+            ea.record(stream)
+            step()
+            eb.record(stream)
+        torch.cuda.synchronize()
+        per_step = sorted(ea.elapsed_time(eb) for ea, eb in evs)
     else:
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
@@ -627,8 +639,15 @@ def main():
             step()
             eb.record(stream)
         torch.cuda.synchronize()
-        ms = sum(ea.elapsed_time(eb) for ea, eb in evs) / args.steps
+        per_step = sorted(ea.elapsed_time(eb) for ea, eb in evs)
+        ms = sum(per_step) / args.steps
     clocks.mark_off()
+    q = lambda f: per_step[min(len(per_step) - 1, int(f * len(per_step)))]
+    step_stats = {"median_ms": statistics.median(per_step), "p10_ms": q(0.1), "p90_ms": q(0.9),
+                  "min_ms": per_step[0], "max_ms": per_step[-1], "n": len(per_step),
+                  "how": ("each step its own event pair after a write of twice L2"
+                          if flush is not None else
+                          "each step its own event pair, back to back, after the timed window")}
     barrier(world)
     torch.cuda.synchronize()
     ms = max_over_ranks(ms, world)
@@ -642,11 +661,19 @@ def main():
     sb = stage_bytes(w)
     if args.gate and not fused:
         raise SystemExit("bench.py: --gate times the fused plan; this workload runs four steps")
+    # launches per step: the fused kernel, plus its states-only pass and the
+    # combine when the plan splits the last partial wave by sequence
+    split = "segments" in plan
+    launches = (3 if split else 1) if fused else 4
     if fused:
-        # one kernel launch per step: its average duration is the timed region's
-        # (events on the launching stream, back-to-back launches)
-        # (gated: the step is the fused kernel and the gate pass, timed together)
-        kname = "ssd_fused+k_gate" if args.gate else "ssd_fused"
+        # the step's launches back to back: their total is the timed region's
+        # (events on the launching stream); the dominant kernel's figures below
+        # are charged the whole step (gated: the gate pass too)
+        kname = "k_ssd_pair" if "k_ssd_pair" in plan else "k_ssd_fused"
+        if split:
+            kname += " (+ states-only pass + combine)"
+        if args.gate:
+            kname += " + k_gate"
         kstats = {kname: ms}
         sb[kname] = path_work(w)[0] + z_bytes
     else:
@@ -677,7 +704,9 @@ def main():
     dom = max(kstats, key=kstats.get)
     pk = peaks()
     achieved = sb[dom] / (kstats[dom] / 1e3) / 1e9
-    traffic = recorded_traffic(dom, w.name)
+    # recorded per step: every launch of the step (the dominant kernel's name
+    # is the record's key)
+    traffic = recorded_traffic(dom.split()[0], w.name)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
                 "algorithmic_bytes": sb[dom], "kernel_ms": kstats[dom],
@@ -807,7 +836,8 @@ def main():
                        (f"inputs {in_bytes / 1e6:.1f} MB fit in L2: a {2 * L2_BYTES / 1e6:.0f} "
                         f"MB write before each timed step, steps timed one by one")},
             "roofline": roofline, "path_roofline": path_roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": ((1 if fused else 4) + (1 if args.gate else 0)) * args.steps,
+            "gpu_launches": (launches + (1 if args.gate else 0)) * args.steps,
+            "step_ms": step_stats,
             "plan": plan, "clocks": clk,
         }
         print(json.dumps(line), flush=True)

@@ -47,7 +47,10 @@
  *   (a device error word, and the static scratch array of
  *   ssd_chunked_fwd_static_scratch) and looks up their addresses once per
  *   device, on first use.  cudaDeviceReset discards them, so do not reset a
- *   device the library has been used on in the same process.
+ *   device the library has been used on in the same process.  The cached
+ *   addresses belong to the context current at that first use: call the
+ *   library from the device's primary context (what the CUDA runtime uses
+ *   by default), not from contexts created with the driver API.
  */
 #ifndef SSD_GB300_H
 #define SSD_GB300_H
