@@ -721,10 +721,26 @@ k_pair_combine(const float *h0, const float *seg_state, const float *seg_decay, 
     const int npairs = H >> 1;
     const size_t slab = size_t(pslab / npairs) * H + 2 * (pslab % npairs) + hh;
     float hv = h0 ? h0[slab * PN + e] : 0.f;
-    for (int sg = 0; sg + 1 < nseg; ++sg) {
-        const size_t j = (size_t(ts) * (nseg - 1) + sg) * 2 + hh;
-        hv = fmaf(exp2f(seg_decay[j]), hv, seg_state[j * PN + e]);
-        seg_hin[((size_t(ts) * nseg + sg + 1) * 2 + hh) * PN + e] = hv;
+    // the loads of eight segments are issued together, then the chain runs
+    for (int sg0 = 0; sg0 + 1 < nseg; sg0 += 8) {
+        float dec[8], st[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int sg = sg0 + u;
+            if (sg + 1 < nseg) {
+                const size_t j = (size_t(ts) * (nseg - 1) + sg) * 2 + hh;
+                dec[u] = seg_decay[j];
+                st[u] = seg_state[j * PN + e];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int sg = sg0 + u;
+            if (sg + 1 < nseg) {
+                hv = fmaf(exp2f(dec[u]), hv, st[u]);
+                seg_hin[((size_t(ts) * nseg + sg + 1) * 2 + hh) * PN + e] = hv;
+            }
+        }
     }
 }
 
