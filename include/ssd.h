@@ -69,7 +69,9 @@ typedef enum {
     SSD_ERR_ALIGNMENT = 3,   /* pointer or stride alignment                  */
     SSD_ERR_WORKSPACE = 4,   /* workspace missing or too small               */
     SSD_ERR_CUDA = 5,        /* a CUDA runtime or launch error               */
-    SSD_ERR_TIMEOUT = 6      /* a device-side bounded wait gave up           */
+    SSD_ERR_TIMEOUT = 6,     /* a device-side bounded wait gave up           */
+    SSD_ERR_DEVICE_BOUNDS = 7 /* a device-side bounds check failed (debug
+                                 build only: libssd_gb300_debug.so)          */
 } ssd_status;
 
 /* SSD_I32 only for the parent and state-slot indices of ssd_state_update_tokens
@@ -92,10 +94,14 @@ const char *ssd_status_string(ssd_status status);
 const char *ssd_last_error_detail(void);
 
 /* Waits for `stream`, then reports (and clears) the device-side error word of
- * the current device: SSD_ERR_TIMEOUT if any kernel of this library gave up a
- * bounded wait since the last call (its outputs are then not valid), SSD_OK
- * otherwise, SSD_ERR_CUDA if CUDA itself reports an error.  This is the only
- * entry point that synchronises; call it where a check is wanted. */
+ * the current device: SSD_ERR_DEVICE_BOUNDS if a kernel of the debug build
+ * (compiled with SSD_DEBUG_BOUNDS) found an index, shared-memory offset or
+ * tensor-memory column out of range (ssd_last_error_detail names the source
+ * file and line of the first one; the access was skipped, not made),
+ * SSD_ERR_TIMEOUT if any kernel gave up a bounded wait since the last call
+ * (its outputs are then not valid), SSD_OK otherwise, SSD_ERR_CUDA if CUDA
+ * itself reports an error.  This is the only entry point that synchronises;
+ * call it where a check is wanted. */
 ssd_status ssd_device_status(void *stream);
 
 /* Test hook for the failure path above: launches one CTA on `stream` whose
@@ -105,6 +111,15 @@ ssd_status ssd_device_status(void *stream);
  * on that stream then returns SSD_ERR_TIMEOUT and clears the word.  Nothing
  * else is in flight in that CTA, so the context stays usable. */
 ssd_status ssd_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
+/* Test hook for the debug build's bounds checks (libssd_gb300_debug.so, built
+ * with SSD_DEBUG_BOUNDS; they stand in for a memory checker): launches one
+ * thread on `stream` that tests an index out of range by construction.  The
+ * check records the failure in the device error word and skips the access
+ * (no memory is touched); the next ssd_device_status on that stream returns
+ * SSD_ERR_DEVICE_BOUNDS naming ssd_selftest.cu and clears the word.  The
+ * normal build returns SSD_ERR_UNSUPPORTED and launches nothing. */
+ssd_status ssd_selftest_bounds_check(void *stream);
 
 /* Bytes of device workspace ssd_chunked_fwd needs for this problem, written
  * to *bytes.  x_dtype is the ssd_dtype of x, B, C.  On the four-step path the

@@ -10,12 +10,15 @@ import os
 import threading
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libssd_gb300.so")
+# SSD_DEBUG_BOUNDS=1 selects the debug build (device-side bounds checks,
+# `python -m state_space_model_gb300.build --debug-bounds`); read at import.
+LIB_PATH = os.path.join(_PKG, "libssd_gb300_debug.so" if os.environ.get("SSD_DEBUG_BOUNDS") == "1"
+                        else "libssd_gb300.so")
 
 SSD_F32, SSD_BF16, SSD_I32 = 0, 1, 2
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED",
           3: "SSD_ERR_ALIGNMENT", 4: "SSD_ERR_WORKSPACE", 5: "SSD_ERR_CUDA",
-          6: "SSD_ERR_TIMEOUT"}
+          6: "SSD_ERR_TIMEOUT", 7: "SSD_ERR_DEVICE_BOUNDS"}
 
 
 class SsdTensor(ctypes.Structure):
@@ -47,6 +50,7 @@ SIGNATURES = {
     "ssd_chunked_fwd_static_scratch": [_T, _T, _T, _T, _T, _T, _T, _I64, _I64, _T, _T, _VP],
     "ssd_device_status": [_VP],
     "ssd_selftest_wait_timeout": [ctypes.c_uint64, _VP],
+    "ssd_selftest_bounds_check": [_VP],
     "ssd_state_update": [_T, _T, _T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _VP],
     "ssd_state_update_tokens": [_T, _T, _T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _T, _T, _T,
                                 _I32, _VP],

@@ -263,6 +263,7 @@ const char *ssd_status_string(ssd_status s) {
         case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE";
         case SSD_ERR_CUDA: return "SSD_ERR_CUDA";
         case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT";
+        case SSD_ERR_DEVICE_BOUNDS: return "SSD_ERR_DEVICE_BOUNDS";
     }
     return "SSD_UNKNOWN_STATUS";
 }
@@ -336,18 +337,35 @@ ssd_status ssd_device_status(void *stream) {
     if ((st = cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)),
                           "stream synchronize")))
         return st;
-    unsigned int v = 0;
-    if ((st = cuda_status(cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost), "read")))
+    unsigned int v[2] = {0, 0};
+    if ((st = cuda_status(cudaMemcpy(v, word, sizeof v, cudaMemcpyDeviceToHost), "read")))
         return st;
-    if (v) {
-        const unsigned int zero = 0;
-        if ((st = cuda_status(cudaMemcpy(word, &zero, sizeof zero, cudaMemcpyHostToDevice),
+    if (v[0]) {
+        const unsigned int zero[2] = {0, 0};
+        if ((st = cuda_status(cudaMemcpy(word, zero, sizeof zero, cudaMemcpyHostToDevice),
                               "clear")))
             return st;
+        if (v[0] & 4u) {
+            static const char *const files[] = {"?", "ssd_fused.cu", "ssd_pair.cu", "ssd_tc.cu",
+                                                "ssd_simt.cu", "ssd_selftest.cu"};
+            const unsigned f = v[1] >> 16;
+            return fail(SSD_ERR_DEVICE_BOUNDS,
+                        "a device bounds check failed (flags 0x%x), first at %s line %u; the "
+                        "access was skipped and outputs since the last check are not valid",
+                        v[0], f < 6 ? files[f] : "?", v[1] & 0xffffu);
+        }
         return fail(SSD_ERR_TIMEOUT, "a kernel gave up a bounded wait (flags 0x%x); outputs of "
-                    "the calls since the last check are not valid", v);
+                    "the calls since the last check are not valid", v[0]);
     }
     return ok();
+}
+
+ssd_status ssd_selftest_bounds_check(void *stream) {
+    if (!ssd::bounds_checks_built())
+        return fail(SSD_ERR_UNSUPPORTED, "bounds checks are compiled only into the debug build "
+                    "(libssd_gb300_debug.so)");
+    return cuda_status(ssd::launch_bounds_selftest(static_cast<cudaStream_t>(stream)),
+                       "bounds self-test");
 }
 
 ssd_status ssd_selftest_wait_timeout(uint64_t limit_ns, void *stream) {

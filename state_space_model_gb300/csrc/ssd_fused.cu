@@ -39,6 +39,8 @@
 // columns, 216.4 KiB of shared memory).
 #include "ptx_sm100.cuh"
 #include "ssd_block_math.cuh"
+#define SSD_DBG_FILE 1u   // kDbgFused
+#include "ssd_debug.cuh"
 #include "ssd_internal.h"
 #include "ssd_tc.cuh"
 #include "ssd_tmap.h"
@@ -75,6 +77,7 @@ struct FusedParams {
     __nv_bfloat16 *y;
     int64_t y_sb, y_sl, y_sh;
     unsigned int *err;
+    int64_t n_dt, n_hs;   // element extents of dt and of h0 / h_final (debug build)
 };
 
 // What only a split launch reads (kept apart so the whole-slab kernel's
@@ -84,6 +87,7 @@ struct SplitParams {
     float *seg_state;     // [tail slabs][nseg - 1][P][N] (states-only pass)
     float *seg_decay;     // [tail slabs][nseg - 1]        (states-only pass)
     int n_whole;
+    int64_t n_seg_state, n_seg_decay, n_seg_hin;   // element extents (debug build)
 };
 
 // Shared memory: the operand tiles first (the 128-byte swizzle pattern repeats
@@ -271,6 +275,13 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             hin = p.h0 ? p.h0 + (size_t(seg) * p.B * p.H + slab) * 8192 : nullptr;
         else
             hin = unit_h_in<kMode>(p, sp, slab);
+        if (hin) {   // the debug build checks the slab's span
+            const bool from_seg = kMode != 0 && sp.seg_hin && hin >= sp.seg_hin &&
+                                  hin < sp.seg_hin + sp.n_seg_hin;
+            if (from_seg ? !SSD_SPAN_OK(p.err, hin, sp.seg_hin, sp.n_seg_hin, 8192)
+                         : !SSD_SPAN_OK(p.err, hin, p.h0, p.n_hs, 8192))
+                hin = nullptr;
+        }
 #pragma unroll
         for (int m = 0; m < 32; ++m)
             hreg[m] = hin ? make_float2(hin[(2 * m) * 128 + r], hin[(2 * m + 1) * 128 + r])
@@ -286,7 +297,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 
     if (warp == 0) {
         // ---------------- TMA producer and the cumulative-sum record ----------------
-        const float Ah = p.A[h];
+        const float Ah = SSD_IDX_OK(p.err, h, p.H) ? p.A[h] : 0.f;
         const float *dtp = p.dt + int64_t(b) * p.dt_sb + h;
         // Event loop, warp-uniform: lane 0 tests the barriers and issues the
         // copies, the whole warp builds the records.  Each stream goes ahead as
@@ -300,7 +311,9 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             for (int qq = 0; qq < 4; ++qq) {
                 const int row = 32 * qq + lane;
                 const int64_t t = t_begin + int64_t(j) * 128 + row;
-                if (j < nblk && t < t_end) ptx::cp_async4(dst + row, dtp + t * p.dt_sl);
+                if (j < nblk && t < t_end &&
+                    SSD_IDX_OK(p.err, int64_t(b) * p.dt_sb + h + t * p.dt_sl, p.n_dt))
+                    ptx::cp_async4(dst + row, dtp + t * p.dt_sl);
                 else dst[row] = 0.f;
             }
             ptx::cp_async_commit();   // one group per record, empty past the end
@@ -510,7 +523,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         const int cfirst = pair ? half : 0, cstep = pair ? 2 : 1, nb = pair ? 2 : 4;
         const int r = 32 * q + lane;
         const uint32_t lane_off = uint32_t(32 * q) << 16;
-        const float Dh = p.D ? p.D[h] : 0.f;
+        const float Dh = p.D && SSD_IDX_OK(p.err, h, p.H) ? p.D[h] : 0.f;
         for (int k = 0; k < (states_only ? 0 : nblk); ++k) {
             const int s = k & 1;
             const uint32_t par = (k >> 1) & 1;
@@ -644,6 +657,9 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             hout = p.h_final ? p.h_final + slab * 8192 : nullptr;
         else
             hout = unit_h_out<kMode>(p, sp, slab);
+        if (hout && !((kMode == 2 && SSD_SPAN_OK(p.err, hout, sp.seg_state, sp.n_seg_state, 8192)) ||
+                      (kMode != 2 && SSD_SPAN_OK(p.err, hout, p.h_final, p.n_hs, 8192))))
+            hout = nullptr;
         if (ok && hout) {
 #pragma unroll
             for (int m = 0; m < 32; ++m) {
@@ -652,7 +668,8 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             }
         }
         if constexpr (states_only) {
-            if (ok && warp == 8 && lane == 0) sp.seg_decay[blockIdx.x] = gsum;
+            if (ok && warp == 8 && lane == 0 && SSD_IDX_OK(p.err, blockIdx.x, sp.n_seg_decay))
+                sp.seg_decay[blockIdx.x] = gsum;
         }
     } else {
         // ---------------- warpgroup Y: y and its TMA store ----------------
@@ -808,12 +825,13 @@ namespace {
 // "The essence of selective scan", in sequence order.  grid (tail, P N / 256).
 __global__ void __launch_bounds__(256)
 k_seg_combine(const float *h0, const float *seg_state, const float *seg_decay, float *seg_hin,
-              int n_whole, int nseg) {
+              int n_whole, int nseg, unsigned int *err, int64_t n_hs, int64_t n_state,
+              int64_t n_decay, int64_t n_hin) {
     constexpr size_t PN = 8192;
     const int ts = blockIdx.x;
     const size_t e = size_t(blockIdx.y) * 256 + threadIdx.x;
     const size_t slab = size_t(n_whole) + ts;
-    float hv = h0 ? h0[slab * PN + e] : 0.f;
+    float hv = h0 && SSD_IDX_OK(err, slab * PN + e, n_hs) ? h0[slab * PN + e] : 0.f;
     // the loads of eight segments are issued together, then the chain runs
     for (int sg0 = 0; sg0 + 1 < nseg; sg0 += 8) {
         float dec[8], st[8];
@@ -822,8 +840,9 @@ k_seg_combine(const float *h0, const float *seg_state, const float *seg_decay, f
             const int sg = sg0 + u;
             if (sg + 1 < nseg) {
                 const size_t j = size_t(ts) * (nseg - 1) + sg;
-                dec[u] = seg_decay[j];
-                st[u] = seg_state[j * PN + e];
+                const bool in = SSD_IDX_OK(err, j, n_decay) && SSD_IDX_OK(err, j * PN + e, n_state);
+                dec[u] = in ? seg_decay[j] : 0.f;
+                st[u] = in ? seg_state[j * PN + e] : 0.f;
             }
         }
 #pragma unroll
@@ -831,7 +850,8 @@ k_seg_combine(const float *h0, const float *seg_state, const float *seg_decay, f
             const int sg = sg0 + u;
             if (sg + 1 < nseg) {
                 hv = fmaf(exp2f(dec[u]), hv, st[u]);
-                seg_hin[(size_t(ts) * nseg + sg + 1) * PN + e] = hv;
+                const size_t o = (size_t(ts) * nseg + sg + 1) * PN + e;
+                if (SSD_IDX_OK(err, o, n_hin)) seg_hin[o] = hv;
             }
         }
     }
@@ -882,6 +902,17 @@ cudaError_t launch_fused(const Args &a, cudaStream_t s) {
     p.y_sl = a.y_sl;
     p.y_sh = a.y_sh;
     p.err = err;
+    {
+        Args ax = a;
+        fill_extents(ax);
+        p.n_dt = ax.n_dt;
+    }
+    p.n_hs = d.B * d.H * 8192;
+    if (f.nseg > 1) {
+        sp.n_seg_state = f.tail * (f.nseg - 1) * 8192;
+        sp.n_seg_decay = f.tail * (f.nseg - 1);
+        sp.n_seg_hin = f.tail * f.nseg * 8192;
+    }
     const int smem = FusedSmem::kBytes;
     const bool split = f.nseg > 1;
     e = split ? cudaFuncSetAttribute(k_ssd_fused<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
@@ -896,7 +927,7 @@ cudaError_t launch_fused(const Args &a, cudaStream_t s) {
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         k_seg_combine<<<dim3(unsigned(f.tail), unsigned(d.P * d.N / 256)), 256, 0, s>>>(
             a.h0, sp.seg_state, sp.seg_decay, reinterpret_cast<float *>(a.ws + f.off_hin),
-            sp.n_whole, f.nseg);
+            sp.n_whole, f.nseg, err, p.n_hs, sp.n_seg_state, sp.n_seg_decay, sp.n_seg_hin);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     const unsigned units = unsigned(f.n_whole) + unsigned(f.tail) * unsigned(f.nseg);

@@ -38,7 +38,35 @@ struct Args {
     int hprev_dt = DT_F32;
     char *ws = nullptr;                       // workspace base (fused path's tail split)
     const void *z = nullptr;   int64_t z_sb = 0, z_sl = 0, z_sh = 0;   // output gate, or null
+    // filled by the launchers: the device error word, and the element extents
+    // (largest index + 1) of the strided tensors, which the debug build's
+    // bounds checks use
+    unsigned int *err = nullptr;
+    int64_t n_x = 0, n_dt = 0, n_b = 0, n_c = 0, n_y = 0;
 };
+
+// Largest element index + 1 of each strided tensor of a (innermost stride 1).
+inline void fill_extents(Args &a) {
+    const Dims &d = a.d;
+    auto ext = [](int64_t n0, int64_t s0, int64_t n1, int64_t s1, int64_t n2, int64_t s2,
+                  int64_t inner) {
+        if (n0 <= 0 || n1 <= 0 || n2 <= 0) return int64_t(0);
+        return (n0 - 1) * s0 + (n1 - 1) * s1 + (n2 - 1) * s2 + inner;
+    };
+    a.n_x = ext(d.B, a.x_sb, d.L, a.x_sl, d.H, a.x_sh, d.P);
+    a.n_y = ext(d.B, a.y_sb, d.L, a.y_sl, d.H, a.y_sh, d.P);
+    a.n_dt = ext(d.B, a.dt_sb, d.L, a.dt_sl, 1, 0, d.H);
+    a.n_b = ext(d.B, a.b_sb, d.L, a.b_sl, d.G, a.b_sg, d.N);
+    a.n_c = ext(d.B, a.c_sb, d.L, a.c_sl, d.G, a.c_sg, d.N);
+}
+
+// A copy of `in` with the device error word and the extents filled in (what
+// the launchers pass to their kernels).
+inline cudaError_t debug_args(const Args &in, Args *out) {
+    *out = in;
+    fill_extents(*out);
+    return device_error_word(&out->err);
+}
 
 
 // y *= silu(z) in place (a.y, a.z with their strides, a.d's B, L, H, P).

@@ -33,6 +33,8 @@
 // role that touches tensor memory is placed accordingly.
 #include "ptx_sm100.cuh"
 #include "ssd_block_math.cuh"
+#define SSD_DBG_FILE 2u   // kDbgPair
+#include "ssd_debug.cuh"
 #include "ssd_internal.h"
 #include "ssd_tc.cuh"
 #include "ssd_tmap.h"
@@ -61,6 +63,8 @@ struct PairParams {
     float *seg_state;     // [tail pairs][nseg - 1][2][P][N] (states-only pass)
     float *seg_decay;     // [tail pairs][nseg - 1][2]        (states-only pass)
     int n_whole;          // whole pair slabs ahead of the split ones
+    // element extents, for the debug build's bounds checks
+    int64_t n_dt, n_hs, n_seg_state, n_seg_decay, n_seg_hin;
 };
 
 constexpr int kPThreads = 640;   // 20 warps; 96 registers per thread
@@ -170,6 +174,9 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     const int h_base = 2 * (pslab % npairs);
     const int g = h_base / p.hpg;
     const int nblk = int((t_end - t_begin + 127) / 128);
+    if (!SSD_IN_BOUNDS(p.err, pslab >= 0 && pslab < p.B * npairs && seg < p.nseg && nblk > 0 &&
+                                  t_end <= p.L && h_base + 1 < p.H))
+        return;   // uniform over the CTA: nothing has started yet
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(&bars[kFullB], 1);
@@ -409,7 +416,7 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         // into ring slot j & 3, four records ahead; each lane copies, and later
         // reads, its own four rows.
         const int hh = warp - 2;
-        const float Ah = p.A[h_base + hh];
+        const float Ah = SSD_IDX_OK(p.err, h_base + hh, p.H) ? p.A[h_base + hh] : 0.f;
         const float *dtp = p.dt + int64_t(b) * p.dt_sb + h_base + hh;
         float *dtring = reinterpret_cast<float *>(smem + SM::kDT) + hh * 512;
         float *rec0 = rec_all + hh * 4 * kPRec;
@@ -419,7 +426,9 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             for (int qq = 0; qq < 4; ++qq) {
                 const int row = 32 * qq + lane;
                 const int64_t t = t_begin + int64_t(j) * 128 + row;
-                if (j < nblk && t < t_end) ptx::cp_async4(dst + row, dtp + t * p.dt_sl);
+                if (j < nblk && t < t_end &&
+                    SSD_IDX_OK(p.err, int64_t(b) * p.dt_sb + h_base + hh + t * p.dt_sl, p.n_dt))
+                    ptx::cp_async4(dst + row, dtp + t * p.dt_sl);
                 else dst[row] = 0.f;
             }
             ptx::cp_async_commit();   // one group per record, empty past the end
@@ -487,7 +496,8 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         }
         ptx::cp_async_wait<0>();
         if constexpr (states_only) {
-            if (ok && lane == 0) p.seg_decay[(size_t(pslab - p.n_whole) * (p.nseg - 1) + seg) * 2 + hh] = gsum;
+            const size_t jd = (size_t(pslab - p.n_whole) * (p.nseg - 1) + seg) * 2 + hh;
+            if (ok && lane == 0 && SSD_IDX_OK(p.err, jd, p.n_seg_decay)) p.seg_decay[jd] = gsum;
         }
     } else if (warp < 12) {
         // ---------------- decay operand L_hh on lane quarter q ----------------
@@ -499,7 +509,7 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         const int q = warp & 3, hh = (warp - 4) >> 2;
         const int r = 32 * q + lane;
         const uint32_t lane_off = uint32_t(32 * q) << 16;
-        const float Dh = p.D ? p.D[h_base + hh] : 0.f;
+        const float Dh = p.D && SSD_IDX_OK(p.err, h_base + hh, p.H) ? p.D[h_base + hh] : 0.f;
         const float *rec0 = rec_all + hh * 4 * kPRec;
         for (int k = 0; k < (states_only ? 0 : nblk); ++k) {
             if (!__all_sync(0xffffffffu,
@@ -573,8 +583,13 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         if (ok) {
             const float *hin;
             if constexpr (kMode == 2) hin = nullptr;
-            else if (seg > 0) hin = p.seg_hin + ((size_t(ts) * p.nseg + seg) * 2 + hh) * 8192;
-            else hin = p.h0 ? p.h0 + (size_t(b) * p.H + h) * 8192 : nullptr;
+            else if (seg > 0) {
+                const size_t o = ((size_t(ts) * p.nseg + seg) * 2 + hh) * 8192;
+                hin = SSD_IDX_OK(p.err, o + 8191, p.n_seg_hin) ? p.seg_hin + o : nullptr;
+            } else {
+                const size_t o = (size_t(b) * p.H + h) * 8192;
+                hin = p.h0 && SSD_IDX_OK(p.err, o + 8191, p.n_hs) ? p.h0 + o : nullptr;
+            }
             const float d0 = ex2(rec0[388]);
             if constexpr (states_only) release_record(0);
 #pragma unroll
@@ -636,9 +651,11 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 d1 = ex2(rec0[kPRec * (k1 & 3) + 388]);
                 if constexpr (states_only) release_record(k1);
             } else if constexpr (kMode == 2) {
-                hout = p.seg_state + ((size_t(ts) * (p.nseg - 1) + seg) * 2 + hh) * 8192;
+                const size_t o = ((size_t(ts) * (p.nseg - 1) + seg) * 2 + hh) * 8192;
+                hout = SSD_IDX_OK(p.err, o + 8191, p.n_seg_state) ? p.seg_state + o : nullptr;
             } else if (seg < 0 || seg == p.nseg - 1) {
-                hout = p.h_final ? p.h_final + (size_t(b) * p.H + h) * 8192 : nullptr;
+                const size_t o = (size_t(b) * p.H + h) * 8192;
+                hout = p.h_final && SSD_IDX_OK(p.err, o + 8191, p.n_hs) ? p.h_final + o : nullptr;
             }
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
@@ -713,14 +730,15 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 // heads, P N / 256).
 __global__ void __launch_bounds__(256)
 k_pair_combine(const float *h0, const float *seg_state, const float *seg_decay, float *seg_hin,
-               int n_whole, int nseg, int H) {
+               int n_whole, int nseg, int H, unsigned int *err, int64_t n_hs, int64_t n_state,
+               int64_t n_decay, int64_t n_hin) {
     constexpr size_t PN = 8192;
     const int ts = blockIdx.x >> 1, hh = blockIdx.x & 1;
     const size_t e = size_t(blockIdx.y) * 256 + threadIdx.x;
     const int pslab = n_whole + ts;
     const int npairs = H >> 1;
     const size_t slab = size_t(pslab / npairs) * H + 2 * (pslab % npairs) + hh;
-    float hv = h0 ? h0[slab * PN + e] : 0.f;
+    float hv = h0 && SSD_IDX_OK(err, slab * PN + e, n_hs) ? h0[slab * PN + e] : 0.f;
     // the loads of eight segments are issued together, then the chain runs
     for (int sg0 = 0; sg0 + 1 < nseg; sg0 += 8) {
         float dec[8], st[8];
@@ -729,8 +747,9 @@ k_pair_combine(const float *h0, const float *seg_state, const float *seg_decay, 
             const int sg = sg0 + u;
             if (sg + 1 < nseg) {
                 const size_t j = (size_t(ts) * (nseg - 1) + sg) * 2 + hh;
-                dec[u] = seg_decay[j];
-                st[u] = seg_state[j * PN + e];
+                const bool in = SSD_IDX_OK(err, j, n_decay) && SSD_IDX_OK(err, j * PN + e, n_state);
+                dec[u] = in ? seg_decay[j] : 0.f;
+                st[u] = in ? seg_state[j * PN + e] : 0.f;
             }
         }
 #pragma unroll
@@ -738,7 +757,8 @@ k_pair_combine(const float *h0, const float *seg_state, const float *seg_decay, 
             const int sg = sg0 + u;
             if (sg + 1 < nseg) {
                 hv = fmaf(exp2f(dec[u]), hv, st[u]);
-                seg_hin[((size_t(ts) * nseg + sg + 1) * 2 + hh) * PN + e] = hv;
+                const size_t o = ((size_t(ts) * nseg + sg + 1) * 2 + hh) * PN + e;
+                if (SSD_IDX_OK(err, o, n_hin)) seg_hin[o] = hv;
             }
         }
     }
@@ -843,6 +863,17 @@ cudaError_t launch_pair(const Args &a, cudaStream_t s) {
     p.h0 = a.h0;
     p.h_final = a.final_states;
     p.err = err;
+    {
+        Args ax = a;
+        fill_extents(ax);
+        p.n_dt = ax.n_dt;
+    }
+    p.n_hs = d.B * d.H * 8192;
+    if (f.nseg > 1) {
+        p.n_seg_state = f.tail * (f.nseg - 1) * 2 * 8192;
+        p.n_seg_decay = f.tail * (f.nseg - 1) * 2;
+        p.n_seg_hin = f.tail * f.nseg * 2 * 8192;
+    }
     const int smem = PairSmem::kBytes;
     if (f.nseg > 1) {
         p.seg_state = reinterpret_cast<float *>(a.ws + f.off_state);
@@ -859,7 +890,7 @@ cudaError_t launch_pair(const Args &a, cudaStream_t s) {
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         k_pair_combine<<<dim3(unsigned(f.tail) * 2, unsigned(d.P * d.N / 256)), 256, 0, s>>>(
             a.h0, p.seg_state, p.seg_decay, reinterpret_cast<float *>(a.ws + f.off_hin),
-            p.n_whole, f.nseg, p.H);
+            p.n_whole, f.nseg, p.H, err, p.n_hs, p.n_seg_state, p.n_seg_decay, p.n_seg_hin);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const unsigned units = unsigned(f.n_whole) + unsigned(f.tail) * unsigned(f.nseg);
         k_ssd_pair<1><<<units, kPThreads, smem, s>>>(tm_x, tm_b, tm_c, tm_y, p);

@@ -9,6 +9,8 @@
 // by log2(e) so every decay is one exp2.
 #include "ssd_internal.h"
 #include "ssd_simt.cuh"
+#define SSD_DBG_FILE 4u   // kDbgSimt
+#include "ssd_debug.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -33,7 +35,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 __global__ void __launch_bounds__(256)
 k_chunk_cumsum(const float *__restrict__ dt, int64_t dt_sb, int64_t dt_sl,
                const float *__restrict__ A, float *__restrict__ G, int64_t L, int H, int Q,
-               int64_t nc) {
+               int64_t nc, unsigned int *err, int64_t n_dt, int64_t n_G) {
     const int64_t c = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y * 8 + warp;
@@ -48,7 +50,9 @@ k_chunk_cumsum(const float *__restrict__ dt, int64_t dt_sb, int64_t dt_sl,
     for (int k = 0; k < 8; ++k) {
         if (k < R) {
             const int64_t t = t0 + k;
-            const float d = (t < L) ? __ldg(dt + b * dt_sb + t * dt_sl + h) : 0.f;
+            const float d = (t < L && SSD_IDX_OK(err, b * dt_sb + t * dt_sl + h, n_dt))
+                                ? __ldg(dt + b * dt_sb + t * dt_sl + h)
+                                : 0.f;
             run += a * d;
             v[k] = run;
         }
@@ -63,7 +67,8 @@ k_chunk_cumsum(const float *__restrict__ dt, int64_t dt_sb, int64_t dt_sl,
     float *g = G + (b * H + h) * (nc * Q) + t0;
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-        if (k < R) g[k] = (excl + v[k]) * kLog2e;
+        if (k < R && SSD_IDX_OK(err, (b * H + h) * (nc * Q) + t0 + k, n_G))
+            g[k] = (excl + v[k]) * kLog2e;
 }
 
 // ---------------------------------------------------------------------------
@@ -81,6 +86,11 @@ __global__ void __launch_bounds__(256) k_chunk_state_simt(Args a) {
     float *xs = sm;               // [32][P], rows scaled by w_j
     float *bs = sm + 32 * P;      // [32][N]
     float *ws = bs + 32 * N;      // [32]
+    // the block's G row and S tile (uniform over the block, before any barrier)
+    if (!SSD_IN_BOUNDS(a.err, (b * d.H + h) * d.Lp() + c * Q + Q <= d.B * d.H * d.Lp() &&
+                                  ((b * d.nc + c) * d.H + h + 1) * int64_t(P) * N <=
+                                      d.B * d.nc * d.H * int64_t(P) * N))
+        return;
     const float *Grow = a.G + (b * d.H + h) * d.Lp() + c * Q;
     const float g_last = Grow[Q - 1];
     const T *x = static_cast<const T *>(a.x);
@@ -96,20 +106,23 @@ __global__ void __launch_bounds__(256) k_chunk_state_simt(Args a) {
     for (int j0 = 0; j0 < Q; j0 += 32) {
         if (threadIdx.x < 32) {
             const int64_t t = c * Q + j0 + threadIdx.x;
-            ws[threadIdx.x] = (t < d.L) ? exp2f(g_last - Grow[j0 + threadIdx.x]) *
-                                              __ldg(a.dt + b * a.dt_sb + t * a.dt_sl + h)
-                                        : 0.f;
+            ws[threadIdx.x] = (t < d.L && SSD_IDX_OK(a.err, b * a.dt_sb + t * a.dt_sl + h, a.n_dt))
+                                  ? exp2f(g_last - Grow[j0 + threadIdx.x]) *
+                                        __ldg(a.dt + b * a.dt_sb + t * a.dt_sl + h)
+                                  : 0.f;
         }
         __syncthreads();
         for (int e = threadIdx.x; e < 32 * P; e += 256) {
             const int jj = e / P, p = e - jj * P;
             const int64_t t = c * Q + j0 + jj;
-            xs[e] = (t < d.L) ? ws[jj] * to_f(x[b * a.x_sb + t * a.x_sl + h * a.x_sh + p]) : 0.f;
+            const int64_t xo = b * a.x_sb + t * a.x_sl + h * a.x_sh + p;
+            xs[e] = (t < d.L && SSD_IDX_OK(a.err, xo, a.n_x)) ? ws[jj] * to_f(x[xo]) : 0.f;
         }
         for (int e = threadIdx.x; e < 32 * N; e += 256) {
             const int jj = e / N, n = e - jj * N;
             const int64_t t = c * Q + j0 + jj;
-            bs[e] = (t < d.L) ? to_f(Bm[b * a.b_sb + t * a.b_sl + g * a.b_sg + n]) : 0.f;
+            const int64_t bo = b * a.b_sb + t * a.b_sl + g * a.b_sg + n;
+            bs[e] = (t < d.L && SSD_IDX_OK(a.err, bo, a.n_b)) ? to_f(Bm[bo]) : 0.f;
         }
         __syncthreads();
 #pragma unroll 4
@@ -157,6 +170,10 @@ __global__ void __launch_bounds__(256) k_state_passing(Args a) {
     const int64_t slab = blockIdx.x, b = slab / d.H, h = slab % d.H;
     const int64_t PN = d.P * d.N;
     const int nq = int(PN >> 2);  // float4 per state, 64..4096
+    if (!SSD_IN_BOUNDS(a.err, (slab + 1) * PN <= d.B * d.H * PN &&
+                                  (slab + 1) * d.Lp() <= d.B * d.H * d.Lp() &&
+                                  ((b * d.nc + d.nc - 1) * d.H + h + 1) * PN <= d.B * d.nc * d.H * PN))
+        return;
     float4 hv[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
@@ -219,6 +236,10 @@ __global__ void __launch_bounds__(256) k_chunk_scan_simt(Args a) {
     const T *x = static_cast<const T *>(a.x);
     const T *Bm = static_cast<const T *>(a.Bm);
     const T *Cm = static_cast<const T *>(a.Cm);
+    if (!SSD_IN_BOUNDS(a.err, (b * d.H + h) * d.Lp() + c * Q + Q <= d.B * d.H * d.Lp() &&
+                                  ((b * d.nc + c) * d.H + h + 1) * int64_t(P) * N <=
+                                      d.B * d.nc * d.H * int64_t(P) * N))
+        return;
     const float *Grow = a.G + (b * d.H + h) * d.Lp() + c * Q;
     const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
     const int TP = P >> 4;
@@ -227,7 +248,8 @@ __global__ void __launch_bounds__(256) k_chunk_scan_simt(Args a) {
     for (int e = threadIdx.x; e < 64 * N; e += 256) {
         const int r = e / N, n = e - r * N;
         const int64_t t = i0 + r;
-        Cs[r * NS + n] = (t < d.L) ? to_f(Cm[b * a.c_sb + t * a.c_sl + g * a.c_sg + n]) : 0.f;
+        const int64_t co = b * a.c_sb + t * a.c_sl + g * a.c_sg + n;
+        Cs[r * NS + n] = (t < d.L && SSD_IDX_OK(a.err, co, a.n_c)) ? to_f(Cm[co]) : 0.f;
     }
     if (threadIdx.x < 64) gi[threadIdx.x] = Grow[rb * 64 + threadIdx.x];
 
@@ -243,14 +265,17 @@ __global__ void __launch_bounds__(256) k_chunk_scan_simt(Args a) {
         for (int e = threadIdx.x; e < 64 * N; e += 256) {
             const int r = e / N, n = e - r * N;
             const int64_t t = j0 + r;
-            Bs[r * NS + n] = (t < d.L) ? to_f(Bm[b * a.b_sb + t * a.b_sl + g * a.b_sg + n]) : 0.f;
+            const int64_t bo = b * a.b_sb + t * a.b_sl + g * a.b_sg + n;
+            Bs[r * NS + n] = (t < d.L && SSD_IDX_OK(a.err, bo, a.n_b)) ? to_f(Bm[bo]) : 0.f;
         }
         for (int e = threadIdx.x; e < 64 * P; e += 256) {
             const int r = e / P, p = e - r * P;
             const int64_t t = j0 + r;
-            Xs[e] = (t < d.L) ? __ldg(a.dt + b * a.dt_sb + t * a.dt_sl + h) *
-                                    to_f(x[b * a.x_sb + t * a.x_sl + h * a.x_sh + p])
-                              : 0.f;
+            const int64_t xo = b * a.x_sb + t * a.x_sl + h * a.x_sh + p;
+            const int64_t dto = b * a.dt_sb + t * a.dt_sl + h;
+            Xs[e] = (t < d.L && SSD_IDX_OK(a.err, xo, a.n_x) && SSD_IDX_OK(a.err, dto, a.n_dt))
+                        ? __ldg(a.dt + dto) * to_f(x[xo])
+                        : 0.f;
         }
         if (threadIdx.x < 64) gj[threadIdx.x] = Grow[jb * 64 + threadIdx.x];
         __syncthreads();
@@ -321,7 +346,7 @@ __global__ void __launch_bounds__(256) k_chunk_scan_simt(Args a) {
             }
         }
     }
-    const float Dh = a.D ? a.D[h] : 0.f;
+    const float Dh = a.D && SSD_IDX_OK(a.err, h, d.H) ? a.D[h] : 0.f;
     T *y = static_cast<T *>(a.y);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -334,8 +359,10 @@ __global__ void __launch_bounds__(256) k_chunk_scan_simt(Args a) {
             if (k < TP) {
                 const int p = tj + 16 * k;
                 const int64_t xo = b * a.x_sb + t * a.x_sl + h * a.x_sh + p;
+                const int64_t yo = b * a.y_sb + t * a.y_sl + h * a.y_sh + p;
+                if (!SSD_IDX_OK(a.err, xo, a.n_x) || !SSD_IDX_OK(a.err, yo, a.n_y)) continue;
                 const float v = fmaf(e, inter[r][k], yacc[r][k]) + Dh * to_f(x[xo]);
-                y[b * a.y_sb + t * a.y_sl + h * a.y_sh + p] = from_f<T>(v);
+                y[yo] = from_f<T>(v);
             }
         }
     }
@@ -343,15 +370,21 @@ __global__ void __launch_bounds__(256) k_chunk_scan_simt(Args a) {
 
 }  // namespace
 
-cudaError_t simt_chunk_cumsum(const Args &a, cudaStream_t s) {
+cudaError_t simt_chunk_cumsum(const Args &a0, cudaStream_t s) {
+    Args a;
+    cudaError_t e0 = debug_args(a0, &a);
+    if (e0 != cudaSuccess) return e0;
     const Dims &d = a.d;
     dim3 grid(unsigned(d.nc), unsigned((d.H + 7) / 8), unsigned(d.B));
     k_chunk_cumsum<<<grid, 256, 0, s>>>(a.dt, a.dt_sb, a.dt_sl, a.A, a.G, d.L, int(d.H),
-                                        int(d.Q), d.nc);
+                                        int(d.Q), d.nc, a.err, a.n_dt, d.B * d.H * d.Lp());
     return cudaGetLastError();
 }
 
-cudaError_t simt_chunk_state(const Args &a, cudaStream_t s) {
+cudaError_t simt_chunk_state(const Args &a0, cudaStream_t s) {
+    Args a;
+    cudaError_t e0 = debug_args(a0, &a);
+    if (e0 != cudaSuccess) return e0;
     const Dims &d = a.d;
     dim3 grid(unsigned(d.nc), unsigned(d.H), unsigned(d.B));
     const size_t smem = sizeof(float) * (32 * d.P + 32 * d.N + 32);
@@ -363,7 +396,10 @@ cudaError_t simt_chunk_state(const Args &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t simt_state_passing(const Args &a, cudaStream_t s) {
+cudaError_t simt_state_passing(const Args &a0, cudaStream_t s) {
+    Args a;
+    cudaError_t e0 = debug_args(a0, &a);
+    if (e0 != cudaSuccess) return e0;
     const Dims &d = a.d;
     dim3 grid(unsigned(d.B * d.H));
     if (a.hprev_dt == DT_F32)
@@ -373,7 +409,10 @@ cudaError_t simt_state_passing(const Args &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t simt_chunk_scan(const Args &a, cudaStream_t s) {
+cudaError_t simt_chunk_scan(const Args &a0, cudaStream_t s) {
+    Args a;
+    cudaError_t e0 = debug_args(a0, &a);
+    if (e0 != cudaSuccess) return e0;
     const Dims &d = a.d;
     dim3 grid(unsigned(d.nc * (d.Q / 64)), unsigned(d.H), unsigned(d.B));
     const size_t smem = sizeof(float) * (2 * 64 * (d.N + 1) + 64 * 65 + 64 * d.P + 128);

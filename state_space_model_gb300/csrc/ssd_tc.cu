@@ -13,6 +13,8 @@
 #include "ptx_sm100.cuh"
 #include "ssd_internal.h"
 #include "ssd_tc.cuh"
+#define SSD_DBG_FILE 3u   // kDbgTc
+#include "ssd_debug.cuh"
 #include "ssd_tmap.h"
 
 #include <cuda.h>
@@ -25,7 +27,7 @@ namespace ssd {
 namespace {
 
 // Set by a kernel whose bounded wait gave up (see ssd_device_status).
-__device__ unsigned int g_device_error;
+__device__ unsigned int g_device_error[2];
 
 constexpr int kTile = 8192;  // one 64-row x 128-byte swizzled tile (bf16 64 x 64)
 
@@ -38,6 +40,7 @@ struct StateTcParams {
     float *S;
     int64_t nc;
     unsigned int *err;
+    int64_t n_dt, n_G, n_S;   // element extents (debug build)
 };
 
 template <int KH, int NSTG>
@@ -109,9 +112,12 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
             const int i = e / Q, j = e - i * Q;
             const float *Grow = p.G + (b * p.H + h0 + i) * p.Lp + c * Q;
             const int64_t t = c * Q + j;
-            wts[e] = (t < p.L) ? exp2f(Grow[Q - 1] - Grow[j]) *
-                                     __ldg(p.dt + b * p.dt_sb + t * p.dt_sl + h0 + i)
-                               : 0.f;
+            const int64_t gb = (b * p.H + h0 + i) * p.Lp + c * Q;
+            const int64_t dto = b * p.dt_sb + t * p.dt_sl + h0 + i;
+            wts[e] = (t < p.L && SSD_IDX_OK(p.err, gb + Q - 1, p.n_G) &&
+                      SSD_IDX_OK(p.err, dto, p.n_dt))
+                         ? exp2f(Grow[Q - 1] - Grow[j]) * __ldg(p.dt + dto)
+                         : 0.f;
         }
     }
     ptx::tc_fence_before();
@@ -196,7 +202,9 @@ k_chunk_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
             const uint32_t row = tmem + (uint32_t(32 * q) << 16);
 #pragma unroll
             for (int i = 0; i < KH; ++i) {
-                float *S = p.S + ((b * p.nc + c) * p.H + h0 + i) * (64 * 128) + n;
+                const int64_t so = ((b * p.nc + c) * p.H + h0 + i) * (64 * 128);
+                if (!SSD_IDX_OK(p.err, so + 64 * 128 - 1, p.n_S)) continue;
+                float *S = p.S + so + n;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     uint32_t r[16];
@@ -242,6 +250,7 @@ struct ScanTcParams {
     __nv_bfloat16 *y;
     int64_t y_sb, y_sl, y_sh;
     unsigned int *err;
+    int64_t n_dt, n_G, n_y;   // element extents (debug build)
 };
 
 template <int QB>
@@ -307,12 +316,14 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     }
     if (warp >= 2) {
         const int i = threadIdx.x - 64;
-        const float *Grow = p.G + (b * p.H + h) * p.Lp + c * Q;
-        gi[i] = Grow[r * 128 + i];
+        const int64_t gb = (b * p.H + h) * p.Lp + c * Q;
+        const float *Grow = p.G + gb;
+        gi[i] = SSD_IDX_OK(p.err, gb + r * 128 + i, p.n_G) ? Grow[r * 128 + i] : 0.f;
         for (int s = 0; s < nblk; ++s) {
             const int64_t t = c * Q + s * 128 + i;
-            gj[s * 128 + i] = Grow[s * 128 + i];
-            dtj[s * 128 + i] = (t < p.L) ? __ldg(p.dt + b * p.dt_sb + t * p.dt_sl + h) : 0.f;
+            const int64_t dto = b * p.dt_sb + t * p.dt_sl + h;
+            gj[s * 128 + i] = SSD_IDX_OK(p.err, gb + s * 128 + i, p.n_G) ? Grow[s * 128 + i] : 0.f;
+            dtj[s * 128 + i] = (t < p.L && SSD_IDX_OK(p.err, dto, p.n_dt)) ? __ldg(p.dt + dto) : 0.f;
         }
     }
     ptx::tc_fence_before();
@@ -447,7 +458,7 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             ptx::tc_fence_after();
             const int64_t t = c * Q + r * 128 + i;
             const float e_i = exp2f(g_i);
-            const float Dh = p.D ? p.D[h] : 0.f;
+            const float Dh = p.D && SSD_IDX_OK(p.err, h, p.H) ? p.D[h] : 0.f;
             const uint8_t *Xrow = smem + SM::kX + r * 16384 + i * 128;
             __nv_bfloat16 *yrow = p.y + b * p.y_sb + t * p.y_sl + int64_t(h) * p.y_sh;
 #pragma unroll 1
@@ -475,7 +486,9 @@ k_chunk_scan_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         __nv_bfloat162 h2 = __floats2bfloat162_rn(y0, y1);
                         o[k] = *reinterpret_cast<uint32_t *>(&h2);
                     }
-                    if (t < p.L)
+                    if (t < p.L &&
+                        SSD_IDX_OK(p.err, b * p.y_sb + t * p.y_sl + int64_t(h) * p.y_sh + 8 * ch + 7,
+                                   p.n_y))
                         *reinterpret_cast<uint4 *>(yrow + 8 * ch) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
             }
@@ -559,8 +572,11 @@ cudaError_t tc_chunk_state(const Args &a, cudaStream_t s) {
     if ((e = make_tmap_bf16_4d(&tm_b, a.Bm, bd, bs, box)) != cudaSuccess) return e;
     unsigned int *err = nullptr;
     if ((e = device_error_word(&err)) != cudaSuccess) return e;
+    Args ax = a;
+    fill_extents(ax);
     StateTcParams p{d.L, d.Lp(), int(d.H), int(d.hpg()), int(d.Q), a.dt, a.dt_sb, a.dt_sl,
-                    a.G, a.S, d.nc, err};
+                    a.G, a.S, d.nc, err, ax.n_dt, d.B * d.H * d.Lp(),
+                    d.B * d.nc * d.H * 64 * 128};
     if (d.hpg() % 2 == 0) {
         auto k = k_chunk_state_tc<2, 2>;
         const int smem = StateTcSmem<2, 2>::kBytes;
@@ -617,7 +633,16 @@ cudaError_t tc_chunk_scan(const Args &a, cudaStream_t s) {
                    a.y_sb,
                    a.y_sl,
                    a.y_sh,
-                   err};
+                   err,
+                   0,
+                   d.B * d.H * d.Lp(),
+                   0};
+    {
+        Args ax = a;
+        fill_extents(ax);
+        p.n_dt = ax.n_dt;
+        p.n_y = ax.n_y;
+    }
     return d.Q == 256 ? launch_scan_tc<2>(a, s, tm_x, tm_b, tm_c, tm_hp, p)
                       : launch_scan_tc<1>(a, s, tm_x, tm_b, tm_c, tm_hp, p);
 }
