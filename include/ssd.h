@@ -180,6 +180,51 @@ ssd_status ssd_chunked_fwd_gated(const ssd_tensor *x, const ssd_tensor *dt,
                                  ssd_tensor *final_states, void *workspace,
                                  size_t workspace_bytes, void *stream);
 
+/* ---- sequence sharding over ranks -------------------------------------------
+ * "mamba-metal", "The essence of selective scan": the recurrence
+ * h_t = a_t h_{t-1} + b_t over a run of tokens composes into one pair
+ * (a, b) = (total decay, state reached from zero), and pairs compose
+ * associatively in sequence order, (a2, b2) o (a1, b1) = (a2 a1, a2 b1 + b2).
+ * A sequence split into contiguous segments, one per rank (rank order =
+ * sequence order), is run as: every rank calls ssd_chunked_fwd on its segment
+ * with no initial state (its y from zero, its final state b) and
+ * ssd_segment_logdecay (log a); the ranks exchange (log a, b); each rank calls
+ * ssd_sequence_combine for the state h_in entering its segment and
+ * ssd_shard_correct, which adds h_in's contribution to y and turns b into the
+ * rank's final state.  The result is the unsplit forward's up to rounding (y
+ * is rounded twice in bf16 runs).  The exchange itself is the caller's (the
+ * Python binding's chunked_fwd_sequence_sharded uses torch.distributed).
+ * Same conventions as ssd_chunked_fwd: device pointers, every check before
+ * any launch, work enqueued on `stream`, no allocation. */
+
+/* logdecay[b, h] = A[h] * sum_t dt[b, t, h] (natural log of the segment's
+ * total decay).  dt [B, L, H] f32 (innermost stride 1), A [H] f32,
+ * logdecay [B, H] f32 contiguous (output). */
+ssd_status ssd_segment_logdecay(const ssd_tensor *dt, const ssd_tensor *A,
+                                ssd_tensor *logdecay, void *stream);
+
+/* h_in = the composition of the pairs of ranks 0 .. rank - 1, applied to
+ * initial_states (or zero): h <- exp(logdecay[q]) h + states[q] for q = 0 ..
+ * rank - 1.  logdecay [R, B, H] f32, states [R, B, H, P, N] f32 (the gathered
+ * pairs of all R ranks), initial_states [B, H, P, N] f32 or NULL (the state
+ * entering the whole sequence), h_in [B, H, P, N] f32 (output), all
+ * contiguous; 0 <= rank < R. */
+ssd_status ssd_sequence_combine(const ssd_tensor *logdecay_all, const ssd_tensor *states_all,
+                                const ssd_tensor *initial_states, int32_t rank,
+                                ssd_tensor *h_in, void *stream);
+
+/* In place: y[b, t, h, :] += exp(cum[b, t, h]) * C[b, t, g, :] . h_in[b, h]^T
+ * with cum the inclusive prefix over the segment of A[h] dt[b, ., h] and g =
+ * h / (H / ngroups), and, if final_states is given, final_states <-
+ * exp(logdecay) h_in + final_states.  y [B, L, H, P] (f32 or bf16; innermost
+ * stride 1) holds the segment's output from a zero state and C [B, L, G, N]
+ * has y's dtype; dt, A as for ssd_chunked_fwd; h_in, final_states
+ * [B, H, P, N] f32 and logdecay [B, H] f32, contiguous. */
+ssd_status ssd_shard_correct(const ssd_tensor *dt, const ssd_tensor *A, const ssd_tensor *C,
+                             const ssd_tensor *h_in, const ssd_tensor *logdecay,
+                             int64_t ngroups, ssd_tensor *y, ssd_tensor *final_states,
+                             void *stream);
+
 /* ---- allocation-free variant ------------------------------------------------
  * The pages have no counterpart of this call; it exists for callers that
  * cannot hand the library a device workspace: code that runs where no

@@ -51,6 +51,9 @@ SIGNATURES = {
     "ssd_device_status": [_VP],
     "ssd_selftest_wait_timeout": [ctypes.c_uint64, _VP],
     "ssd_selftest_bounds_check": [_VP],
+    "ssd_segment_logdecay": [_T, _T, _T, _VP],
+    "ssd_sequence_combine": [_T, _T, _T, _I32, _T, _VP],
+    "ssd_shard_correct": [_T, _T, _T, _T, _T, _I64, _T, _T, _VP],
     "ssd_state_update": [_T, _T, _T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _VP],
     "ssd_state_update_tokens": [_T, _T, _T, _T, _T, _T, _T, _T, _T, _I32, _I64, _T, _T, _T, _T,
                                 _I32, _VP],

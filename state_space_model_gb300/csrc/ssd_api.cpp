@@ -984,3 +984,131 @@ ssd_status ssd_stage_chunk_scan(const ssd_tensor *x, const ssd_tensor *dt, const
 }
 
 }  // extern "C"
+
+/* ---- sequence sharding over ranks ---------------------------------------- */
+
+namespace ssd {
+cudaError_t launch_segment_logdecay(const float *dt, int64_t dt_sb, int64_t dt_sl, const float *A,
+                                    int64_t B, int64_t L, int64_t H, float *out, cudaStream_t s);
+cudaError_t launch_sequence_combine(const float *logdecay, const float *states, const float *h0,
+                                    int rank, int64_t BH, int64_t PN, float *h_in, cudaStream_t s);
+cudaError_t launch_shard_correct(const Args &a, const float *h_in, const float *logdecay,
+                                 cudaStream_t s);
+}  // namespace ssd
+
+ssd_status ssd_segment_logdecay(const ssd_tensor *dt, const ssd_tensor *A, ssd_tensor *logdecay,
+                                void *stream) {
+    if (!dt || dt->ndim != 3) return fail(SSD_ERR_INVALID_ARG, "dt: missing or ndim != 3");
+    const int64_t Bn = dt->shape[0], L = dt->shape[1], H = dt->shape[2];
+    if (Bn < 0 || L < 0 || H <= 0 || H > 65535 || Bn > 65535)
+        return fail(SSD_ERR_INVALID_ARG, "dt: shape (%lld, %lld, %lld) out of range",
+                    (long long)Bn, (long long)L, (long long)H);
+    const int64_t sdt[3] = {Bn, L, H}, sh[1] = {H}, so[2] = {Bn, H};
+    ssd_status st;
+    if ((st = check_tensor(dt, "dt", 3, sdt, SSD_F32, false, false))) return st;
+    if ((st = check_tensor(A, "A", 1, sh, SSD_F32, true, false))) return st;
+    if ((st = check_tensor(logdecay, "logdecay", 2, so, SSD_F32, true, false))) return st;
+    const Range ro = range_of(logdecay);
+    if (overlap(ro, range_of(dt)) || overlap(ro, range_of(A)))
+        return fail(SSD_ERR_INVALID_ARG, "logdecay overlaps an input");
+    if (Bn == 0) return ok();
+    if ((st = check_device_ptrs({{dt->data, "dt"}, {A->data, "A"}, {logdecay->data, "logdecay"}})))
+        return st;
+    if ((st = cuda_status(ssd::launch_segment_logdecay(
+                              static_cast<const float *>(dt->data), dt->stride[0], dt->stride[1],
+                              static_cast<const float *>(A->data), Bn, L, H,
+                              static_cast<float *>(logdecay->data),
+                              static_cast<cudaStream_t>(stream)),
+                          "segment log-decay")))
+        return st;
+    return ok();
+}
+
+ssd_status ssd_sequence_combine(const ssd_tensor *logdecay_all, const ssd_tensor *states_all,
+                                const ssd_tensor *initial_states, int32_t rank, ssd_tensor *h_in,
+                                void *stream) {
+    if (!states_all || states_all->ndim != 5)
+        return fail(SSD_ERR_INVALID_ARG, "states: missing or ndim != 5");
+    const int64_t R = states_all->shape[0], Bn = states_all->shape[1], H = states_all->shape[2],
+                  P = states_all->shape[3], N = states_all->shape[4];
+    if (R <= 0 || rank < 0 || rank >= R)
+        return fail(SSD_ERR_INVALID_ARG, "rank %d outside [0, %lld)", rank, (long long)R);
+    const int64_t sl[3] = {R, Bn, H}, ss[5] = {R, Bn, H, P, N}, sh[4] = {Bn, H, P, N};
+    ssd_status st;
+    if ((st = check_tensor(logdecay_all, "logdecay", 3, sl, SSD_F32, true, false))) return st;
+    if ((st = check_tensor(states_all, "states", 5, ss, SSD_F32, true, false))) return st;
+    if (initial_states &&
+        (st = check_tensor(initial_states, "initial_states", 4, sh, SSD_F32, true, false)))
+        return st;
+    if ((st = check_tensor(h_in, "h_in", 4, sh, SSD_F32, true, false))) return st;
+    const Range ro = range_of(h_in);
+    if (overlap(ro, range_of(logdecay_all)) || overlap(ro, range_of(states_all)) ||
+        overlap(ro, range_of(initial_states)))
+        return fail(SSD_ERR_INVALID_ARG, "h_in overlaps an input");
+    if (Bn * H * P * N == 0) return ok();
+    if ((st = check_device_ptrs({{logdecay_all->data, "logdecay"}, {states_all->data, "states"},
+                                 {initial_states ? initial_states->data : nullptr,
+                                  "initial_states"},
+                                 {h_in->data, "h_in"}})))
+        return st;
+    if ((st = cuda_status(ssd::launch_sequence_combine(
+                              static_cast<const float *>(logdecay_all->data),
+                              static_cast<const float *>(states_all->data),
+                              initial_states ? static_cast<const float *>(initial_states->data)
+                                             : nullptr,
+                              rank, Bn * H, P * N, static_cast<float *>(h_in->data),
+                              static_cast<cudaStream_t>(stream)),
+                          "sequence combine")))
+        return st;
+    return ok();
+}
+
+ssd_status ssd_shard_correct(const ssd_tensor *dt, const ssd_tensor *A, const ssd_tensor *Cm,
+                             const ssd_tensor *h_in, const ssd_tensor *logdecay, int64_t ngroups,
+                             ssd_tensor *y, ssd_tensor *final_states, void *stream) {
+    if (!y || !Cm) return fail(SSD_ERR_INVALID_ARG, "y / C: null tensor descriptor");
+    if (y->ndim != 4 || Cm->ndim != 4) return fail(SSD_ERR_INVALID_ARG, "y / C: ndim must be 4");
+    const int64_t Bn = y->shape[0], L = y->shape[1], H = y->shape[2], P = y->shape[3];
+    const int64_t N = Cm->shape[3], Gn = ngroups;
+    ssd_status st = check_geometry(Bn, L, H, P, N, Gn, 256);
+    if (st != SSD_OK) return st;
+    const int xdt = y->dtype;
+    const int64_t sy[4] = {Bn, L, H, P}, sdt[3] = {Bn, L, H}, sc[4] = {Bn, L, Gn, N},
+                  sh[1] = {H}, sst[4] = {Bn, H, P, N}, sld[2] = {Bn, H};
+    if ((st = check_tensor(y, "y", 4, sy, -1, false, false))) return st;
+    if ((st = check_tensor(dt, "dt", 3, sdt, SSD_F32, false, false))) return st;
+    if ((st = check_tensor(A, "A", 1, sh, SSD_F32, true, false))) return st;
+    if ((st = check_tensor(Cm, "C", 4, sc, xdt, false, false))) return st;
+    if ((st = check_tensor(h_in, "h_in", 4, sst, SSD_F32, true, false))) return st;
+    if ((st = check_tensor(logdecay, "logdecay", 2, sld, SSD_F32, true, false))) return st;
+    if (final_states &&
+        (st = check_tensor(final_states, "final_states", 4, sst, SSD_F32, true, false)))
+        return st;
+    const Range ry = range_of(y), rf = range_of(final_states);
+    const Range ins[] = {range_of(dt), range_of(A), range_of(Cm), range_of(h_in),
+                         range_of(logdecay)};
+    for (const Range &r : ins)
+        if (overlap(ry, r) || overlap(rf, r))
+            return fail(SSD_ERR_INVALID_ARG, "an output overlaps an input");
+    if (overlap(ry, rf)) return fail(SSD_ERR_INVALID_ARG, "y overlaps final_states");
+    if (Bn == 0) return ok();
+    if ((st = check_device_ptrs({{dt->data, "dt"}, {A->data, "A"}, {Cm->data, "C"},
+                                 {h_in->data, "h_in"}, {logdecay->data, "logdecay"},
+                                 {y->data, "y"},
+                                 {final_states ? final_states->data : nullptr, "final_states"}})))
+        return st;
+    ssd::Args a;
+    a.d = ssd::Dims{Bn, L, H, P, N, Gn, 256, (L + 255) / 256};
+    a.xdt = xdt;
+    fill_dt(a, dt);
+    a.A = static_cast<const float *>(A->data);
+    fill_bc(a, nullptr, Cm);
+    fill_y(a, y);
+    a.final_states = final_states ? static_cast<float *>(final_states->data) : nullptr;
+    if ((st = cuda_status(ssd::launch_shard_correct(a, static_cast<const float *>(h_in->data),
+                                                    static_cast<const float *>(logdecay->data),
+                                                    static_cast<cudaStream_t>(stream)),
+                          "shard correction")))
+        return st;
+    return ok();
+}
