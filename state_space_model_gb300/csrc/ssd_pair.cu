@@ -771,7 +771,11 @@ bool pair_supported(const Dims &d, int xdt) {
         const char *e = std::getenv("SSD_NO_PAIR");
         return e && e[0] == '1';
     }();
-    return !off && fused_supported(d, xdt) && d.H % 2 == 0 && d.hpg() % 2 == 0;
+    // Two heads per CTA halve the number of units; with fewer pair slabs than
+    // SMs the single-head kernel keeps more SMs busy (and splits by sequence
+    // less), and it measured faster on every such workload.
+    return !off && fused_supported(d, xdt) && d.H % 2 == 0 && d.hpg() % 2 == 0 &&
+           d.B * d.H / 2 >= device_sm_count();
 }
 
 // Cost model in units of one pair-block (128 tokens of two heads) on one SM.

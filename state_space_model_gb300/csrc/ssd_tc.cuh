@@ -28,8 +28,9 @@ int device_sm_count();   // of the current device; 152 when there is none
 cudaError_t launch_fused(const Args &a, cudaStream_t s);
 
 // The pair kernel (ssd_pair.cu): the fused forward over two heads of one group
-// per CTA; needs H and the heads per group even.  Splits the pair slabs left
-// over after the last full wave by sequence, with the same workspace record.
+// per CTA; taken when H and the heads per group are even and there are at
+// least as many pair slabs as SMs.  Splits the pair slabs left over after the
+// last full wave by sequence, with the same workspace record.
 bool pair_supported(const Dims &d, int xdt);
 FusedSplit pair_split(const Dims &d, int sm_count);
 cudaError_t launch_pair(const Args &a, cudaStream_t s);

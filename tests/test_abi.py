@@ -154,8 +154,7 @@ def test_fused_split_plan(lib):
     PN = 64 * 128
     M = 152   # SM count assumed without a device
     # (B, L, H, G): two heads per CTA (heads per group even)
-    for B, L, H, G in [(1, 65536, 8, 1), (1, 16384, 4, 1), (1, 32768, 24, 1), (8, 4096, 80, 1),
-                       (1, 16384, 128, 8)]:
+    for B, L, H, G in [(8, 4096, 80, 1), (3, 4096, 102, 1), (1, 20000, 308, 2)]:
         plan = d(B, L, H, 64, 128, G, 256, BF16)
         assert "k_ssd_pair" in plan, plan
         m = re.search(r"(\d+) whole \(batch, head pair\) slabs \+ the last (\d+) pair slabs in "
@@ -170,8 +169,9 @@ def test_fused_split_plan(lib):
         assert lib.ssd_workspace_size(B, L, H, 64, 128, G, 256, BF16, ctypes.byref(out)) == 0
         assert out.value == ws, (plan, out.value, ws)
         assert f"workspace {ws} bytes" in plan
-    # one head per CTA (odd heads per group)
-    for B, L, H in [(1, 65536, 3), (2, 8000, 3), (1, 32768, 25)]:
+    # one head per CTA: odd heads per group, or fewer pair slabs than SMs
+    for B, L, H in [(1, 65536, 3), (2, 8000, 3), (1, 32768, 25), (1, 65536, 8), (1, 16384, 4),
+                    (1, 32768, 24)]:
         plan = d(B, L, H, 64, 128, 1, 256, BF16)
         assert "k_ssd_fused" in plan, plan
         m = re.search(r"the last (\d+) slabs in (\d+) segments of (\d+) tokens", plan)
@@ -191,6 +191,7 @@ def test_fused_split_plan(lib):
         assert out.value == 0
     assert "k_ssd_fused" in d(2, 4096, 153, 64, 128, 1, 256, BF16)   # odd heads per group
     assert "k_ssd_pair" in d(2, 4096, 152, 64, 128, 1, 256, BF16)
+    assert "k_ssd_fused" in d(2, 4096, 150, 64, 128, 1, 256, BF16)   # 150 pair slabs < 152 SMs
 
 
 def test_error_paths(lib):

@@ -23,8 +23,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 # (dtype, B, L, H, G, Q, initial states, environment): every plan of the forward
 CASES = [
-    ("bf16", 2, 640, 8, 2, 256, True, {}),                          # pair kernel, whole slabs
-    ("bf16", 1, 8000, 4, 2, 256, True, {}),                         # pair kernel, sequence split
+    ("bf16", 2, 640, 152, 2, 256, True, {}),                        # pair kernel, whole slabs
+    ("bf16", 1, 3000, 308, 2, 256, True, {}),                       # pair kernel, sequence split
     ("bf16", 2, 1000, 3, 1, 256, True, {}),                         # single-head kernel, split
     ("bf16", 3, 389, 6, 6, 128, False, {}),                         # single-head kernel, whole
     ("bf16", 2, 700, 4, 2, 128, True, {"SSD_FORCE_STAGED": "1"}),   # staged tcgen05 steps

@@ -147,9 +147,10 @@ E2E_CASES = [
     ("bf16", 1, 300, 2, 128, 128, 1, 128, True),
     ("bf16", 1, 77, 2, 16, 32, 1, 256, True),
     # fused bf16 path with one head per group (ngroups = nheads: the single-head
-    # kernel) and two heads per group (the pair kernel), ragged L
+    # kernel) and two heads per group (the pair kernel: a full wave of pair
+    # slabs), ragged L
     ("bf16", 2, 1000, 6, 64, 128, 6, 256, True),
-    ("bf16", 3, 777, 8, 64, 128, 4, 128, True),
+    ("bf16", 2, 777, 152, 64, 128, 76, 128, True),
 ]
 
 
@@ -217,9 +218,10 @@ def test_plan_names_the_kernel():
     """Two heads per CTA where the heads per group are even, one otherwise."""
     m = ssd()
     assert "k_ssd_pair" in m.describe_plan(8, 4096, 80, 64, 128, 1, 256)
-    assert "k_ssd_pair" in m.describe_plan(1, 16384, 128, 64, 128, 8, 128)
+    assert "k_ssd_pair" in m.describe_plan(2, 777, 152, 64, 128, 76, 128)
     assert "k_ssd_fused" in m.describe_plan(2, 1000, 6, 64, 128, 6, 256)
     assert "k_ssd_fused" in m.describe_plan(2, 1000, 3, 64, 128, 1, 256)
+    assert "k_ssd_fused" in m.describe_plan(1, 16384, 128, 64, 128, 8, 128)   # 64 pair slabs
 
 
 def test_plan_choice():
@@ -348,7 +350,7 @@ def test_resume_at_chunk_boundary_is_exact(dtype):
     np.testing.assert_array_equal(f2, f)
 
 
-@pytest.mark.parametrize("B,H,L,G", [(1, 4, 8000, 2), (2, 3, 5000, 1)])
+@pytest.mark.parametrize("B,H,L,G", [(1, 4, 8000, 2), (2, 3, 5000, 1), (1, 308, 4000, 2)])
 def test_fused_split_matches_oracle(B, H, L, G):
     """Few slabs over a long sequence: each slab runs as sequence segments on
     separate SMs, started from the combined states of a states-only pass.
