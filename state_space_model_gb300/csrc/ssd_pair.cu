@@ -16,21 +16,24 @@
 // through the state, as in the single-head fused kernel (ssd_fused.cu), with
 // the same per-block record, decay operand and skip term on the diagonal.
 //
-// Tensor memory (512 columns): [0, 128) C B^T, then L_0 and L_1 written in
-// place (32-column block c holds L_0 of tokens 32c.. in its first 16 columns
-// and L_1 in its last 16); [128, 256) the fp32 state of both heads (lanes =
-// state index n, columns = (head, headdim)), which holds 2^(g_end) h(k) before
-// S^T(k) adds onto it, so it holds h(k + 1) after; [256 + 128 s, +128) the y
-// accumulator of stage s (blocks alternate).  The state never leaves tensor
-// memory: the state update is a read, one multiply and a write back.
+// Tensor memory (512 columns): [128 s, +128) C B^T of the blocks of stage s
+// (blocks alternate), then L_0 and L_1 written in place (32-column block c
+// holds L_0 of tokens 32c.. in its first 16 columns and L_1 in its last 16),
+// so that C B^T(k + 1) and its decay operand are formed while L x(k) waits for
+// its inputs; [256, 384) the fp32 state of both heads (lanes = state index n,
+// columns = (head, headdim)), which holds 2^(g_end) h(k) before S^T(k) adds
+// onto it, so it holds h(k + 1) after; [384, 512) the y accumulator.  The
+// state never leaves tensor memory: the state update is a read, one multiply
+// and a write back.
 //
-// Roles (20 warps): warp 0 = TMA producer; warp 1 = tensor-memory owner and
-// MMA issuer (one thread, an event loop); warps 2, 3 = the cumulative-sum
-// record of head 0, 1; warps 4..11 = the decay operand (warp 4 + 4 hh + q
-// builds L_hh on lane quarter q); warps 12..19 = head warps (warp 12 + 4 hh +
-// q: w o x, the scale of inter, the state update and the y drain of head hh on
-// lane quarter q).  A warp reaches tensor-memory lanes 32 (warp % 4) ..; every
-// role that touches tensor memory is placed accordingly.
+// Roles (20 warps): warp 0 = TMA producer (B, C, x loads, y stores); warp 1 =
+// tensor-memory owner and MMA issuer (one thread, an event loop); warps 2, 3 =
+// the cumulative-sum record and w o x of head 0, 1; warps 4..11 = the decay
+// operand (warp 4 + 4 hh + q builds L_hh on lane quarter q); warps 12..19 =
+// head warps (warp 12 + 4 hh + q: the scale of inter, the state update and the
+// y drain of head hh on lane quarter q).  A warp reaches tensor-memory lanes
+// 32 (warp % 4) ..; every role that touches tensor memory is placed
+// accordingly.
 #include "ptx_sm100.cuh"
 #include "ssd_block_math.cuh"
 #define SSD_DBG_FILE 2u   // kDbgPair
@@ -89,9 +92,20 @@ static_assert(PairSmem::kF % 16 == 0 && PairSmem::kDT % 16 == 0 && PairSmem::kBa
               "alignment");
 
 // Tensor-memory columns.
-constexpr uint32_t kTL = 0;     // C B^T / L_0, L_1
-constexpr uint32_t kTS = 128;   // state
-constexpr uint32_t kTY = 256;   // y accumulator, two stages of 128
+constexpr uint32_t kTL = 0;     // C B^T / L_0, L_1, two stages of 128
+constexpr uint32_t kTS = 256;   // state
+constexpr uint32_t kTY = 384;   // y accumulator
+
+// v[m] *= f for 32 fp32 values, as 16 packed multiplies.
+__device__ __forceinline__ void scale32(uint32_t (&v)[32], float f) {
+    const float2 f2 = make_float2(f, f);
+#pragma unroll
+    for (int m = 0; m < 32; m += 2) {
+        const float2 r = __fmul2_rn(make_float2(__uint_as_float(v[m]), __uint_as_float(v[m + 1])), f2);
+        v[m] = __float_as_uint(r.x);
+        v[m + 1] = __float_as_uint(r.y);
+    }
+}
 
 // A warp-uniform bounded wait: false if any lane's wait gave up.
 __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
@@ -128,20 +142,21 @@ __device__ __forceinline__ void pair_unit(const PairParams &p, int &pslab, int &
 // tcgen05.commit) mark a product's completion; the others count arrivals.
 enum : int {
     kFullB = 0, kFullC = 1,            // TMA landed (single buffers)
-    kCbDone = 2, kSDone = 3,           // C B^T(k), S^T(k) completed
-    kLReady = 4,                       // L(k) built (256 threads)
-    kWReady = 5,                       // w o x(k) written (64 threads: the record warps)
-    kSReady = 6,                       // 2^(g_end) h(k) in the state columns (256 threads)
-    kHbReady = 7,                      // bf16 h(k) written (256 threads)
-    kInterDone = 8,                    // [2] C h^T(k) completed
-    kScaled = 10,                      // [2] inter(k) scaled in place (256 threads)
-    kIntraDone = 12,                   // [2] L x(k) completed: y(k) complete
-    kYFree = 14,                       // [2] y(k) read out of tensor memory (256 threads)
-    kFullX = 16,                       // [2] x(k) landed in slot k & 1
-    kSlotDone = 18,                    // [2] slot k & 1: y(k) staged in it (256 threads), or
+    kCbDone = 2,                       // [2] C B^T(k) completed (stage k & 1)
+    kSDone = 4,                        // S^T(k) completed
+    kLReady = 5,                       // [2] L(k) built (256 threads)
+    kWReady = 7,                       // w o x(k) written (64 threads: the record warps)
+    kSReady = 8,                       // 2^(g_end) h(k) in the state columns (256 threads)
+    kHbReady = 9,                      // bf16 h(k) written (256 threads)
+    kInterDone = 10,                   // C h^T(k) completed
+    kScaled = 11,                      // inter(k) scaled in place (256 threads)
+    kIntraDone = 12,                   // [2] L x(k) completed: y(k) complete (stage k & 1)
+    kYFree = 14,                       // y(k) read out of tensor memory (256 threads)
+    kFullX = 15,                       // [2] x(k) landed in slot k & 1
+    kSlotDone = 17,                    // [2] slot k & 1: y(k) staged in it (256 threads), or
                                        // in the states-only pass w o x(k) has read x(k) (64)
-    kScReady = 20,                     // [2 heads][4] record ready (32 lanes)
-    kRecFree = 28,                     // [2 heads][4] record released by its readers
+    kScReady = 19,                     // [2 heads][4] record ready (32 lanes)
+    kRecFree = 27,                     // [2 heads][4] record released by its readers
 };
 
 template <int kMode>
@@ -181,17 +196,17 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     if (threadIdx.x == 0) {
         ptx::mbar_init(&bars[kFullB], 1);
         ptx::mbar_init(&bars[kFullC], 1);
-        ptx::mbar_init(&bars[kCbDone], 1);
         ptx::mbar_init(&bars[kSDone], 1);
-        ptx::mbar_init(&bars[kLReady], 256);
         ptx::mbar_init(&bars[kWReady], 64);
         ptx::mbar_init(&bars[kSReady], 256);
         ptx::mbar_init(&bars[kHbReady], 256);
+        ptx::mbar_init(&bars[kInterDone], 1);
+        ptx::mbar_init(&bars[kScaled], 256);
+        ptx::mbar_init(&bars[kYFree], 256);
         for (int s = 0; s < 2; ++s) {
-            ptx::mbar_init(&bars[kInterDone + s], 1);
-            ptx::mbar_init(&bars[kScaled + s], 256);
+            ptx::mbar_init(&bars[kCbDone + s], 1);
+            ptx::mbar_init(&bars[kLReady + s], 256);
             ptx::mbar_init(&bars[kIntraDone + s], 1);
-            ptx::mbar_init(&bars[kYFree + s], 256);
             ptx::mbar_init(&bars[kFullX + s], 1);
             ptx::mbar_init(&bars[kSlotDone + s], states_only ? 64 : 256);
         }
@@ -220,12 +235,11 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     if (warp == 0) {
         // ---------------- TMA producer and the y stores ----------------
         // Event loop: lane 0 tests the barriers and issues each stream's next
-        // copy as soon as its buffer is free; the warp stays converged and
-        // sleeps briefly when nothing is ready, leaving the issue slots of its
-        // scheduler to the math warps.  Slot k & 1 holds x(k), then y(k): once
-        // y(k) is staged the producer stores it, waits until the store has read
-        // the slot and loads x(k + 2) into it (the states-only pass has no y:
-        // the slot is reloaded once w o x(k) has read x(k)).
+        // copy as soon as its buffer is free; the warp stays converged.  Slot
+        // k & 1 holds x(k), then y(k): once y(k) is staged the producer stores
+        // it, waits until the store has read the slot and loads x(k + 2) into
+        // it (the states-only pass has no y: the slot is reloaded once w o x(k)
+        // has read x(k)).
         auto load_x = [&](int k) {
             const int slot = k & 1;
             const int t0 = int(t_begin + int64_t(k) * 128);
@@ -250,25 +264,35 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             if (lane == 0) {
                 // B(k): read by C B^T(k - 1) and S^T(k - 1) until they complete
                 if (kb < nblk) {
-                    const uint32_t pp = (kb - 1) & 1;
-                    if (kb == 0 || ((states_only || ptx::mbar_test_wait(&bars[kCbDone], pp)) &&
-                                    ptx::mbar_test_wait(&bars[kSDone], pp))) {
+                    const int km = kb - 1;
+                    if (kb == 0 ||
+                        ((states_only ||
+                          ptx::mbar_test_wait(&bars[kCbDone + (km & 1)], (km >> 1) & 1)) &&
+                         ptx::mbar_test_wait(&bars[kSDone], km & 1))) {
                         const int t0 = int(t_begin + int64_t(kb) * 128);
                         ptx::mbar_arrive_expect_tx(&bars[kFullB], 32768);
                         ptx::tma_load_4d(smem + SM::kB, &tm_b, &bars[kFullB], 0, g, t0, b);
                         ptx::tma_load_4d(smem + SM::kB + 16384, &tm_b, &bars[kFullB], 64, g, t0, b);
+                        if (kb + 2 < nblk) {   // start DRAM on the tile two blocks on
+                            ptx::tma_prefetch_l2_4d(&tm_b, 0, g, t0 + 256, b);
+                            ptx::tma_prefetch_l2_4d(&tm_b, 64, g, t0 + 256, b);
+                        }
                         fired |= 1;
                     }
                 }
                 // C(k): read by C B^T(k - 1) and C h^T(k - 1)
                 if (kc < nblk) {
                     const int km = kc - 1;
-                    if (kc == 0 || (ptx::mbar_test_wait(&bars[kCbDone], km & 1) &&
-                                    ptx::mbar_test_wait(&bars[kInterDone + (km & 1)], (km >> 1) & 1))) {
+                    if (kc == 0 || (ptx::mbar_test_wait(&bars[kCbDone + (km & 1)], (km >> 1) & 1) &&
+                                    ptx::mbar_test_wait(&bars[kInterDone], km & 1))) {
                         const int t0 = int(t_begin + int64_t(kc) * 128);
                         ptx::mbar_arrive_expect_tx(&bars[kFullC], 32768);
                         ptx::tma_load_4d(smem + SM::kC, &tm_c, &bars[kFullC], 0, g, t0, b);
                         ptx::tma_load_4d(smem + SM::kC + 16384, &tm_c, &bars[kFullC], 64, g, t0, b);
+                        if (kc + 2 < nblk) {
+                            ptx::tma_prefetch_l2_4d(&tm_c, 0, g, t0 + 256, b);
+                            ptx::tma_prefetch_l2_4d(&tm_c, 64, g, t0 + 256, b);
+                        }
                         fired |= 2;
                     }
                 }
@@ -326,8 +350,8 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 if (k_lx < k_cb && k_lx < k_ch) {
                     const int s = k_lx & 1;
                     const uint32_t ps = (k_lx >> 1) & 1;
-                    if (ptx::mbar_test_wait(&bars[kLReady], k_lx & 1) &&
-                        ptx::mbar_test_wait(&bars[kScaled + s], ps) &&
+                    if (ptx::mbar_test_wait(&bars[kLReady + s], ps) &&
+                        ptx::mbar_test_wait(&bars[kScaled], k_lx & 1) &&
                         ptx::mbar_test_wait(&bars[kFullX + s], ps)) {
                         ptx::tc_fence_after();
                         const uint64_t x0 = dX + uint64_t(s * 2048);
@@ -335,44 +359,45 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                         for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
                             for (int ks = 0; ks < 8; ++ks)
-                                ptx::mma_bf16_ts(tmem + kTY + 128 * s + 64 * hh,
-                                                 tmem + kTL + 32 * (ks >> 1) + 8 * (ks & 1) + 16 * hh,
+                                ptx::mma_bf16_ts(tmem + kTY + 64 * hh,
+                                                 tmem + kTL + 128 * s + 32 * (ks >> 1) + 8 * (ks & 1) +
+                                                     16 * hh,
                                                  x0 + uint64_t(hh * 1024 + ks * 128), kIdLX, 1);
                         ptx::mma_commit(&bars[kIntraDone + s]);
                         ++k_lx;
                         progress = true;
                     }
                 }
-                // C B^T(k): B, C landed and L x(k - 1) has completed (it read L(k - 1))
-                if (k_cb < nblk && (k_cb == 0 || k_lx >= k_cb)) {
-                    const int km = k_cb - 1;
+                // C B^T(k) into stage k & 1: B, C landed and L x(k - 2) has
+                // completed (it read L(k - 2) from that stage)
+                if (k_cb < nblk && (k_cb < 2 || k_lx >= k_cb - 1)) {
+                    const int s = k_cb & 1;
                     if (ptx::mbar_test_wait(&bars[kFullB], k_cb & 1) &&
                         ptx::mbar_test_wait(&bars[kFullC], k_cb & 1) &&
-                        (k_cb == 0 ||
-                         ptx::mbar_test_wait(&bars[kIntraDone + (km & 1)], (km >> 1) & 1))) {
+                        (k_cb < 2 ||
+                         ptx::mbar_test_wait(&bars[kIntraDone + s], ((k_cb - 2) >> 1) & 1))) {
                         ptx::tc_fence_after();
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks)
-                            ptx::mma_bf16_ss(tmem + kTL, dCk + kKoff[ks], dBk + kKoff[ks], kIdCB,
-                                             ks != 0);
-                        ptx::mma_commit(&bars[kCbDone]);
+                            ptx::mma_bf16_ss(tmem + kTL + 128 * s, dCk + kKoff[ks], dBk + kKoff[ks],
+                                             kIdCB, ks != 0);
+                        ptx::mma_commit(&bars[kCbDone + s]);
                         ++k_cb;
                         progress = true;
                     }
                 }
-                // C h^T(k): C landed, bf16 h(k) written, y stage free (y(k - 2) drained)
+                // C h^T(k): C landed, bf16 h(k) written, y accumulator free
+                // (y(k - 1) drained)
                 if (k_ch < nblk) {
-                    const int s = k_ch & 1;
                     if (ptx::mbar_test_wait(&bars[kFullC], k_ch & 1) &&
                         ptx::mbar_test_wait(&bars[kHbReady], k_ch & 1) &&
-                        (k_ch < 2 ||
-                         ptx::mbar_test_wait(&bars[kYFree + s], ((k_ch >> 1) - 1) & 1))) {
+                        (k_ch == 0 || ptx::mbar_test_wait(&bars[kYFree], (k_ch - 1) & 1))) {
                         ptx::tc_fence_after();
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks)   // MN-major state: K step 16 rows = 2 KB
-                            ptx::mma_bf16_ss(tmem + kTY + 128 * s, dCk + kKoff[ks],
-                                             dHB + uint64_t(ks * 128), kIdCH, ks != 0);
-                        ptx::mma_commit(&bars[kInterDone + s]);
+                            ptx::mma_bf16_ss(tmem + kTY, dCk + kKoff[ks], dHB + uint64_t(ks * 128),
+                                             kIdCH, ks != 0);
+                        ptx::mma_commit(&bars[kInterDone]);
                         ++k_ch;
                         progress = true;
                     }
@@ -514,19 +539,20 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         for (int k = 0; k < (states_only ? 0 : nblk); ++k) {
             if (!__all_sync(0xffffffffu,
                             ptx::mbar_wait(&bars[kScReady + hh * 4 + (k & 3)], (k >> 2) & 1) &&
-                                ptx::mbar_wait(&bars[kCbDone], k & 1))) {
+                                ptx::mbar_wait(&bars[kCbDone + (k & 1)], (k >> 1) & 1))) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
             const float *rec = rec0 + kPRec * (k & 3);
             const float gr = rec[r];
+            const uint32_t t_l = tmem + kTL + 128 * (k & 1) + lane_off;
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t out[16];
                 if (c <= q) {
                     uint32_t v[32];
-                    ptx::tmem_ld32(tmem + kTL + 32 * c + lane_off, v);
+                    ptx::tmem_ld32(t_l + 32 * c, v);
                     ptx::tmem_ld_wait();
                     ptx::tc_fence_before();
                     asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
@@ -537,11 +563,11 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) out[jj] = 0u;
                 }
-                ptx::tmem_st16(tmem + kTL + 32 * c + 16 * hh + lane_off, out);
+                ptx::tmem_st16(t_l + 32 * c + 16 * hh, out);
             }
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&bars[kLReady]);
+            ptx::mbar_arrive(&bars[kLReady + (k & 1)]);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&bars[kRecFree + hh * 4 + (k & 3)]);
         }
@@ -613,10 +639,10 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         for (int k = 0; k < nblk && ok; ++k) {
             const int s = k & 1;
             const uint32_t ps = (k >> 1) & 1;
-            const uint32_t t_y = tmem + kTY + 128 * s + 64 * hh + lane_off;   // this row's y columns
+            const uint32_t t_y = tmem + kTY + 64 * hh + lane_off;   // this row's y columns
             if constexpr (!states_only) {
                 // 1. inter(k) = C h^T(k), scaled in place by 2^(g_r); L x(k) adds onto it
-                if (!wait_all(&bars[kInterDone + s], ps)) { ok = false; break; }
+                if (!wait_all(&bars[kInterDone], k & 1)) { ok = false; break; }
                 ptx::tc_fence_after();
                 const float e = ex2(rec0[kPRec * (k & 3) + r]);
                 release_record(k);
@@ -625,13 +651,12 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     uint32_t a[32];
                     ptx::tmem_ld32(t_y + 32 * cb, a);
                     ptx::tmem_ld_wait();
-#pragma unroll
-                    for (int m = 0; m < 32; ++m) a[m] = __float_as_uint(__uint_as_float(a[m]) * e);
+                    scale32(a, e);
                     ptx::tmem_st32(t_y + 32 * cb, a);
                 }
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
-                ptx::mbar_arrive(&bars[kScaled + s]);
+                ptx::mbar_arrive(&bars[kScaled]);
             }
             // 2. h(k + 1) is in the state columns once S^T(k) has completed: keep
             // its bf16 copy for C h^T(k + 1) (C h^T(k) has read the old one) and
@@ -664,8 +689,7 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 ptx::tmem_ld_wait();
                 if (!last) {
                     if constexpr (!states_only) write_hb(cb, v);
-#pragma unroll
-                    for (int m = 0; m < 32; ++m) v[m] = __float_as_uint(__uint_as_float(v[m]) * d1);
+                    scale32(v, d1);
                     ptx::tmem_st32(t_state + 32 * cb, v);
                 } else if (hout) {
 #pragma unroll
@@ -706,7 +730,7 @@ k_ssd_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     put(cb, a);
                 }
                 ptx::tc_fence_before();
-                ptx::mbar_arrive(&bars[kYFree + s]);
+                ptx::mbar_arrive(&bars[kYFree]);
                 ptx::fence_proxy_async_smem();
                 ptx::mbar_arrive(&bars[kSlotDone + s]);
             }
