@@ -148,7 +148,9 @@ ssd_status check_geometry(int64_t B, int64_t L, int64_t H, int64_t P, int64_t N,
 // four-step path with its intermediates in the workspace.
 struct Plan {
     bool fused;
+    bool f32_split;   // fp32 on the tensor cores: bf16 hi / lo copies follow h_prev
     size_t off_G, off_S, off_hp, total;
+    size_t off_x_hi, off_x_lo, off_b_hi, off_b_lo, off_c_hi, off_c_lo, off_hp_hi, off_hp_lo;
 };
 
 Plan plan_workspace(const ssd::Dims &d, int xdt) {
@@ -168,6 +170,20 @@ Plan plan_workspace(const ssd::Dims &d, int xdt) {
     p.off_S = align256(p.off_G + g);
     p.off_hp = align256(p.off_S + s);
     p.total = align256(p.off_hp + hp);
+    p.f32_split = ssd::f32_split_plan(d, xdt);
+    if (p.f32_split) {
+        const size_t xb = size_t(d.B) * d.L * d.H * d.P * 2, bb = size_t(d.B) * d.L * d.G * d.N * 2,
+                     hb = size_t(d.B) * d.nc * d.H * d.P * d.N * 2;
+        p.off_x_hi = p.total;
+        p.off_x_lo = align256(p.off_x_hi + xb);
+        p.off_b_hi = align256(p.off_x_lo + xb);
+        p.off_b_lo = align256(p.off_b_hi + bb);
+        p.off_c_hi = align256(p.off_b_lo + bb);
+        p.off_c_lo = align256(p.off_c_hi + bb);
+        p.off_hp_hi = align256(p.off_c_lo + bb);
+        p.off_hp_lo = align256(p.off_hp_hi + hb);
+        p.total = align256(p.off_hp_lo + hb);
+    }
     return p;
 }
 
@@ -320,6 +336,11 @@ const char *ssd_describe_plan(int64_t batch, int64_t seqlen, int64_t nheads, int
                      "fused: k_ssd_fused x %lld CTAs ((batch, head) slabs), 128-token blocks, "
                      "tcgen05 + TMA, no workspace",
                      (long long)(batch * nheads));
+    } else if (ssd::f32_split_plan(d, x_dtype)) {
+        snprintf(buf, sizeof buf,
+                 "staged: fp32 as bf16 hi + lo copies (k_split_hilo), chunk_cumsum simt, "
+                 "chunk_state tcgen05 (k_chunk_state_tc_f32, three products), state_passing simt, "
+                 "chunk_scan tcgen05 (k_chunk_scan_tc_f32, three products)");
     } else {
         snprintf(buf, sizeof buf,
                  "staged: chunk_cumsum simt, chunk_state %s, state_passing simt, chunk_scan %s",
@@ -347,12 +368,12 @@ ssd_status ssd_device_status(void *stream) {
             return st;
         if (v[0] & 4u) {
             static const char *const files[] = {"?", "ssd_fused.cu", "ssd_pair.cu", "ssd_tc.cu",
-                                                "ssd_simt.cu", "ssd_selftest.cu"};
+                                                "ssd_simt.cu", "ssd_selftest.cu", "ssd_tc_f32.cu"};
             const unsigned f = v[1] >> 16;
             return fail(SSD_ERR_DEVICE_BOUNDS,
                         "a device bounds check failed (flags 0x%x), first at %s line %u; the "
                         "access was skipped and outputs since the last check are not valid",
-                        v[0], f < 6 ? files[f] : "?", v[1] & 0xffffu);
+                        v[0], f < 7 ? files[f] : "?", v[1] & 0xffffu);
         }
         return fail(SSD_ERR_TIMEOUT, "a kernel gave up a bounded wait (flags 0x%x); outputs of "
                     "the calls since the last check are not valid", v[0]);
@@ -479,6 +500,11 @@ ssd_status chunked_fwd_impl(const ssd_tensor *x, const ssd_tensor *dt, const ssd
     a.h_prev = ws + plan.off_hp;
     a.hprev_dt = xdt;
     a.ws = ws;
+    if (plan.f32_split) {
+        a.f32_split = true;
+        a.f32s = {ws + plan.off_x_hi, ws + plan.off_x_lo, ws + plan.off_b_hi, ws + plan.off_b_lo,
+                  ws + plan.off_c_hi, ws + plan.off_c_lo, ws + plan.off_hp_hi, ws + plan.off_hp_lo};
+    }
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (plan.fused) {
@@ -490,6 +516,8 @@ ssd_status chunked_fwd_impl(const ssd_tensor *x, const ssd_tensor *dt, const ssd
         return ok();
     }
     if (L > 0) {
+        if (a.f32_split && (st = cuda_status(ssd::split_inputs_f32(a, s), "fp32 hi/lo split")))
+            return st;
         if ((st = cuda_status(ssd::launch_chunk_cumsum(a, s), "chunk_cumsum"))) return st;
         if ((st = cuda_status(ssd::launch_chunk_state(a, s), "chunk_state"))) return st;
     }

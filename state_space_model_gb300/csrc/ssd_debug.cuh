@@ -20,7 +20,7 @@ constexpr unsigned kErrBounds = 4u;   // a debug-build bounds check failed
 
 // File codes of the kernels' translation units (word 1 holds code << 16 | line).
 enum : unsigned {
-    kDbgFused = 1, kDbgPair = 2, kDbgTc = 3, kDbgSimt = 4, kDbgSelftest = 5,
+    kDbgFused = 1, kDbgPair = 2, kDbgTc = 3, kDbgSimt = 4, kDbgSelftest = 5, kDbgTcF32 = 6,
 };
 
 #ifdef SSD_DEBUG_BOUNDS

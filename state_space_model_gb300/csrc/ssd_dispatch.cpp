@@ -1,6 +1,8 @@
 // Picks the kernel variant of each step for the problem's dtype and geometry:
 // the tensor-core kernels for bf16 inputs with P = 64, N = 128 (and Q of 128
-// or 256 for chunk_scan), the CUDA-core kernels for everything else.
+// or 256 for chunk_scan) and, in the full forward, for fp32 inputs with
+// P = 64, N = 128, Q of 128 or 256 (as bf16 hi / lo pairs); the CUDA-core
+// kernels for everything else.
 #include "ssd_internal.h"
 #include "ssd_simt.cuh"
 #include "ssd_tc.cuh"
@@ -33,6 +35,7 @@ bool use_fused(const Dims &d, int xdt) {
 }
 
 bool uses_tc_chunk_state(const Args &a) { return !force_simt() && tc_chunk_state_supported(a); }
+bool f32_split_plan(const Dims &d, int xdt) { return !force_simt() && tc_f32_supported(d, xdt); }
 bool uses_tc_chunk_scan(const Args &a) { return !force_simt() && tc_chunk_scan_supported(a); }
 
 cudaError_t launch_chunk_cumsum(const Args &a, cudaStream_t s) { return simt_chunk_cumsum(a, s); }

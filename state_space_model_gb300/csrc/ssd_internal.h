@@ -38,6 +38,14 @@ struct Args {
     int hprev_dt = DT_F32;
     char *ws = nullptr;                       // workspace base (fused path's tail split)
     const void *z = nullptr;   int64_t z_sb = 0, z_sl = 0, z_sh = 0;   // output gate, or null
+    // fp32 inputs on the tensor cores (ssd_tc_f32.cu): contiguous bf16 hi / lo
+    // copies of x, B, C and h_prev in the workspace; only the full forward
+    // provides them (f32_split), so the per-step entry points keep the
+    // CUDA-core kernels for fp32
+    bool f32_split = false;
+    struct {
+        void *x_hi, *x_lo, *b_hi, *b_lo, *c_hi, *c_lo, *hp_hi, *hp_lo;
+    } f32s{};
     // filled by the launchers: the device error word, and the element extents
     // (largest index + 1) of the strided tensors, which the debug build's
     // bounds checks use
@@ -80,6 +88,11 @@ bool use_fused(const Dims &d, int xdt);
 // Which variant the four-step path picks for chunk_state / chunk_scan.
 bool uses_tc_chunk_state(const Args &a);
 bool uses_tc_chunk_scan(const Args &a);
+// True when the four-step forward runs fp32 inputs on the tensor cores (the
+// inputs split into bf16 hi / lo copies in the workspace first).
+bool f32_split_plan(const Dims &d, int xdt);
+// Writes the bf16 hi / lo copies of x, B, C (a.f32s) for the fp32 tensor-core steps.
+cudaError_t split_inputs_f32(const Args &a, cudaStream_t stream);
 
 // Kernel launchers (one per step).  Each picks its kernel variant for the
 // geometry and dtype, launches on `stream` and returns the launch status.

@@ -556,10 +556,12 @@ cudaError_t device_error_word(unsigned int **out) {
 }
 
 bool tc_chunk_state_supported(const Args &a) {
+    if (a.xdt == DT_F32) return a.f32_split && tc_f32_supported(a.d, a.xdt);
     return a.xdt == DT_BF16 && a.d.P == 64 && a.d.N == 128 && a.d.Q % 64 == 0 && a.d.Q <= 256;
 }
 
 cudaError_t tc_chunk_state(const Args &a, cudaStream_t s) {
+    if (a.xdt == DT_F32) return tc_chunk_state_f32(a, s);
     const Dims &d = a.d;
     CUtensorMap tm_x, tm_b;
     const uint64_t xd[4] = {64, uint64_t(d.H), uint64_t(d.L), uint64_t(d.B)};
@@ -594,11 +596,14 @@ cudaError_t tc_chunk_state(const Args &a, cudaStream_t s) {
 }
 
 bool tc_chunk_scan_supported(const Args &a) {
+    if (a.xdt == DT_F32)
+        return a.f32_split && a.hprev_dt == DT_F32 && tc_f32_supported(a.d, a.xdt);
     return a.xdt == DT_BF16 && a.hprev_dt == DT_BF16 && a.d.P == 64 && a.d.N == 128 &&
            (a.d.Q == 128 || a.d.Q == 256);
 }
 
 cudaError_t tc_chunk_scan(const Args &a, cudaStream_t s) {
+    if (a.xdt == DT_F32) return tc_chunk_scan_f32(a, s);
     const Dims &d = a.d;
     CUtensorMap tm_x, tm_b, tm_c, tm_hp;
     const uint32_t box[4] = {64, 1, 128, 1};

@@ -8,6 +8,11 @@ bool tc_chunk_state_supported(const Args &a);
 cudaError_t tc_chunk_state(const Args &a, cudaStream_t s);
 bool tc_chunk_scan_supported(const Args &a);
 cudaError_t tc_chunk_scan(const Args &a, cudaStream_t s);
+// fp32 inputs as bf16 hi / lo pairs, three products each (ssd_tc_f32.cu):
+// P = 64, N = 128, Q of 128 or 256, with the split copies in a.f32s.
+bool tc_f32_supported(const Dims &d, int xdt);
+cudaError_t tc_chunk_state_f32(const Args &a, cudaStream_t s);
+cudaError_t tc_chunk_scan_f32(const Args &a, cudaStream_t s);
 }  // namespace ssd
 
 namespace ssd {

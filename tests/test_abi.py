@@ -134,6 +134,9 @@ def test_describe_plan(lib):
     assert d(8, 4096, 80, 64, 128, 1, 256, BF16).startswith("fused")
     assert d(1, 256, 4, 16, 16, 1, 64, F32).startswith("staged")
     assert "tcgen05" in d(2, 300, 4, 64, 128, 1, 64, BF16)
+    f32 = d(2, 300, 4, 64, 128, 1, 128, F32)   # fp32 on the tensor cores as bf16 hi / lo
+    assert "k_chunk_state_tc_f32" in f32 and "k_chunk_scan_tc_f32" in f32, f32
+    assert "tcgen05" not in d(2, 300, 4, 64, 128, 1, 64, F32)   # Q = 64: CUDA-core steps
     assert d(1, 10, 4, 64, 128, 1, 100, BF16).startswith("rejected")
     assert d(1, 10, 4, 64, 128, 1, 64, 9).startswith("rejected")
 

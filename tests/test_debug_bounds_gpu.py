@@ -29,7 +29,8 @@ CASES = [
     ("bf16", 3, 389, 6, 6, 128, False, {}),                         # single-head kernel, whole
     ("bf16", 2, 700, 4, 2, 128, True, {"SSD_FORCE_STAGED": "1"}),   # staged tcgen05 steps
     ("bf16", 1, 1000, 4, 4, 64, True, {}),                          # staged: tc state, simt scan
-    ("f32", 2, 333, 6, 3, 128, True, {}),                           # staged CUDA-core steps
+    ("f32", 2, 333, 6, 3, 128, True, {}),                           # staged fp32 tensor-core steps
+    ("f32", 2, 333, 6, 3, 128, True, {"SSD_FORCE_SIMT": "1"}),      # staged CUDA-core steps
 ]
 
 CHILD = r"""

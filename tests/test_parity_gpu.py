@@ -138,8 +138,13 @@ def test_stage_parity(w):
 E2E_CASES = [
     # (dtype, B, L, H, P, N, G, Q, h0)
     ("f32", 1, 256, 4, 16, 16, 1, 64, False),
-    ("f32", 2, 333, 6, 64, 128, 3, 128, True),
     ("f32", 1, 130, 2, 128, 32, 2, 64, True),
+    # fp32 on the tensor cores (P = 64, N = 128, Q of 128 or 256: bf16 hi / lo
+    # pairs, three products each), two or one head per chunk_state CTA
+    ("f32", 2, 333, 6, 64, 128, 3, 128, True),
+    ("f32", 1, 700, 4, 64, 128, 2, 256, True),
+    ("f32", 2, 1000, 3, 64, 128, 1, 128, False),
+    ("f32", 1, 129, 2, 64, 128, 2, 256, True),
     ("bf16", 2, 700, 4, 64, 128, 1, 256, True),
     ("bf16", 3, 389, 8, 64, 128, 2, 128, False),
     ("bf16", 1, 1000, 4, 64, 128, 4, 64, True),
@@ -388,3 +393,25 @@ def test_fused_many_slabs_match_oracle(B, H, L, G):
         for h in range(H):
             assert rel(y[b, :, h], yr[b, :, h]) <= TOL["bf16"], (b, h)
             assert rel(fin[b, h], fr[b, h]) <= TOL["bf16"], (b, h)
+
+
+def test_f32_tensor_core_plan_and_per_slab_parity():
+    """fp32 inputs at P = 64, N = 128 run chunk_state and chunk_scan on the
+    tensor cores (bf16 hi / lo copies, three products per MMA); the plan names
+    the kernels, and every (b, h) slab meets the fp32 bar against the fp64
+    recurrence."""
+    import os
+    if os.environ.get("SSD_FORCE_SIMT") == "1":
+        pytest.skip("SSD_FORCE_SIMT=1 selects the CUDA-core steps")
+    w = gen.small_case("f32", batch=2, seqlen=900, nheads=4, headdim=64, dstate=128, ngroups=2,
+                       chunk_size=256, init_states=True, seed=4711)
+    plan = ssd().describe_plan(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups,
+                               w.chunk_size, w.torch_dtype)
+    assert "k_chunk_state_tc_f32" in plan and "k_chunk_scan_tc_f32" in plan, plan
+    inp = gen.make_inputs(w)
+    y, f = run(w, inp)
+    yr, fr = oracle_full(w, inp)
+    for b in range(w.batch):
+        for h in range(w.nheads):
+            assert rel(y[b, :, h], yr[b, :, h]) < TOL["f32"], (b, h)
+            assert rel(f[b, h], fr[b, h]) < TOL["f32"], (b, h)
