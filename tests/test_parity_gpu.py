@@ -145,6 +145,8 @@ E2E_CASES = [
     ("f32", 1, 700, 4, 64, 128, 2, 256, True),
     ("f32", 2, 1000, 3, 64, 128, 1, 128, False),
     ("f32", 1, 129, 2, 64, 128, 2, 256, True),
+    ("f32", 2, 1, 2, 64, 128, 1, 128, True),      # one token: a single partial block
+    ("f32", 1, 255, 4, 64, 128, 4, 256, False),   # one token short of a chunk
     ("bf16", 2, 700, 4, 64, 128, 1, 256, True),
     ("bf16", 3, 389, 8, 64, 128, 2, 128, False),
     ("bf16", 1, 1000, 4, 64, 128, 4, 64, True),
