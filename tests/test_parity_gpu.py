@@ -241,8 +241,9 @@ def test_plan_choice():
 # edge cases
 
 
-def test_empty_sequence_returns_initial_state():
-    w = gen.small_case("bf16", batch=2, seqlen=0, nheads=4, ngroups=2, chunk_size=128)
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_empty_sequence_returns_initial_state(dtype):
+    w = gen.small_case(dtype, batch=2, seqlen=0, nheads=4, ngroups=2, chunk_size=128)
     inp = gen.make_inputs(w)
     y, f = run(w, inp)
     assert y.shape == (2, 0, 4, 64)
@@ -252,8 +253,9 @@ def test_empty_sequence_returns_initial_state():
     np.testing.assert_array_equal(f, 0.0)
 
 
-def test_empty_batch():
-    w = gen.small_case("bf16", batch=0, seqlen=100, nheads=4, ngroups=2, chunk_size=128)
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_empty_batch(dtype):
+    w = gen.small_case(dtype, batch=0, seqlen=100, nheads=4, ngroups=2, chunk_size=128)
     inp = gen.make_inputs(w)
     y, f = run(w, inp)
     assert y.shape[0] == 0 and f.shape[0] == 0
@@ -266,6 +268,17 @@ def test_short_and_ragged_sequences(L):
     y, f = run(w, inp)
     yr, fr = oracle_full(w, inp)
     assert rel(y, yr) < TOL["bf16"] and rel(f, fr) < TOL["bf16"]
+
+
+@pytest.mark.parametrize("L", [1, 127, 128, 129])
+def test_short_and_ragged_sequences_f32_tensor_cores(L):
+    """fp32 at P = 64, N = 128, Q = 128 (the tensor-core steps with bf16 hi / lo
+    copies) around one chunk."""
+    w = gen.small_case("f32", batch=1, seqlen=L, nheads=2, ngroups=1, chunk_size=128)
+    inp = gen.make_inputs(w)
+    y, f = run(w, inp)
+    yr, fr = oracle_full(w, inp)
+    assert rel(y, yr) < TOL["f32"] and rel(f, fr) < TOL["f32"]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
