@@ -125,8 +125,11 @@ ssd_status ssd_selftest_bounds_check(void *stream);
  * to *bytes.  x_dtype is the ssd_dtype of x, B, C.  On the four-step path the
  * workspace holds the scaled in-chunk cumulative sums G [B, H, nc*Q] f32, the
  * per-chunk states [B, nc, H, P, N] f32 and the chunk-entering states
- * [B, nc, H, P, N] in the dtype of x.  The fused path needs none, except when
- * there are fewer (batch, head) slabs than SMs and it splits them by
+ * [B, nc, H, P, N] in the dtype of x; for f32 inputs with P = 64, N = 128 and
+ * Q of 128 or 256 (chunk_state and chunk_scan on the tensor cores) it also
+ * holds bf16 hi / lo copies of x, B, C and the chunk-entering states.  The
+ * fused path needs none, except when the (batch, head) or (batch, head pair)
+ * slabs do not fill whole waves of SMs and it splits the remainder by
  * sequence: then it holds each segment's local state, decay and entering
  * state (at most 64 MiB; ssd_describe_plan names the split).  The answer
  * depends on the SM count of the current device.  Returns
