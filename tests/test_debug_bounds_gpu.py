@@ -101,6 +101,36 @@ def test_debug_build_runs_every_plan_without_a_bounds_failure(debug_lib, case):
         assert out["plan"].startswith("staged") and "tcgen05" in out["plan"], out["plan"]
 
 
+FULL = r"""
+import ctypes, json, sys
+import torch
+sys.path.insert(0, sys.argv[1])
+from state_space_model_gb300 import _native, inputs as gen, ssd
+assert _native.LIB_PATH.endswith("libssd_gb300_debug.so"), _native.LIB_PATH
+lib = _native.load()
+w = gen.WORKLOADS[sys.argv[2]]
+inp = gen.make_inputs(w)
+d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+y, f = ssd.chunked_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["initial_states"],
+                       w.chunk_size, w.ngroups)
+torch.cuda.synchronize()
+st = lib.ssd_device_status(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+print(json.dumps({"status": st, "detail": lib.ssd_last_error_detail().decode(),
+                  "finite": bool(torch.isfinite(y.float()).all() and torch.isfinite(f).all())}))
+"""
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "mamba2_130m", "mamba2_2p7b", "hybrid_g8",
+                                  "long_64k"])
+def test_debug_build_at_full_size(debug_lib, name):
+    """Every workload at its full size, in the plan the benchmark times,
+    through the bounds-checked build: no check fires (parity at full size is
+    tested on the normal build)."""
+    out = _child(FULL, name)
+    assert out["status"] == 0, out["detail"]
+    assert out["finite"]
+
+
 def test_debug_build_reports_a_failed_check(debug_lib):
     out = _child(SELFTEST)
     assert out["launch"] == 0
